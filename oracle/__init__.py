@@ -1,0 +1,19 @@
+"""CPU oracle for paged decode attention, slot writes and block copies.
+
+TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference legs may import this package. The product
+path (the CUDA library and its Python binding) never imports it, and the two
+share no code.
+"""
+from .oracle import (  # noqa: F401
+    DTYPE_CODES,
+    build,
+    copy_blocks,
+    kv_cache_write,
+    locate,
+    max_threads,
+    num_blocks,
+    paged_decode,
+    paged_decode_partitioned,
+    slot,
+)
