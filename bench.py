@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode hot path on one or more GPUs.
+
+One step = one decode pass over a synthetic batch: the copy-on-write block copies (where
+the batch has shared blocks), the slot write of every sequence's new token, and paged
+decode attention (split partitions merged by log-sum-exp in the same launch).  The KV
+pool is device-resident state, as in a serving engine; each step's per-step inputs are
+the query, block tables, context lengths and the new tokens.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2]
+    python bench.py --impl reference ...      # the fp64 CPU oracle on the host cores
+
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are independent replicas: each
+rank runs the full batch and the value is the sum of all ranks' bytes over the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "paged decode attention KV-read GB/s (% of HBM peak) and queries/s per batch"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) per launch of the decode kernel, from one ncu capture per
+# workload, valid only for the kernel source whose hash is recorded beside it.
+MEASURED_TRAFFIC: dict = {}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
+                   help="decode batch (default 2: 13B-like MHA, batch 64)")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--partition", type=int, default=-1,
+                   help="partition size in tokens (-1: the batch's own, 0: library default)")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="CPU time budget of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------------
+# workload
+# ------------------------------------------------------------------------------------------
+
+def bench_workload(cfg: int) -> synth.Workload:
+    """The decode batch of config ``cfg`` with the per-step writes of a decode step."""
+    w = synth.config_workload(cfg)
+    if cfg == 4:
+        # the copy-on-write state is built once; each step re-copies the shared partial
+        # block and writes every sequence's next token into its private copy
+        w.info["setup_slots"] = w.slot_mapping
+        w.info["setup_k"], w.info["setup_v"] = w.k_new, w.v_new
+        suffix = (w.context_lens - w.info["prefix_tokens"]).astype(np.int64)
+        starts = np.concatenate([[0], np.cumsum(suffix)[:-1]])  # first suffix token per seq
+        w.slot_mapping = w.info["setup_slots"][starts]
+        w.k_new = w.info["setup_k"][starts]
+        w.v_new = w.info["setup_v"][starts]
+    elif w.k_new is None:
+        synth.add_new_tokens(w, seed=synth.BASE_SEED + 100 + cfg)
+    return w
+
+
+def algorithmic_bytes(w: synth.Workload) -> dict:
+    """Bytes the decode launch must move at minimum, and its parts."""
+    e = w.elem_bytes
+    kv = w.kv_bytes()
+    q = w.q.size * e
+    out = q
+    nblocks = int(sum((int(L) + w.block_size - 1) // w.block_size for L in w.context_lens))
+    tables = nblocks * 4
+    lens = w.num_seqs * 4
+    return {"kv": kv, "q": q, "out": out, "block_tables": tables, "context_lens": lens,
+            "total": kv + q + out + tables + lens}
+
+
+def describe(w: synth.Workload, cfg: int, part: int) -> dict:
+    pool = 2 * w.k_cache.nbytes
+    d = {"workload": w.name, "recipe": synth.CONFIGS[cfg], "batch": w.num_seqs,
+         "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+         "block_size": w.block_size, "partition_tokens": part if part > 0 else 512,
+         "context_tokens": int(w.context_lens.sum()),
+         "context_min_mean_max": [int(w.context_lens.min()), float(w.context_lens.mean()),
+                                  int(w.context_lens.max())],
+         "pool_bytes": pool,
+         "l2": f"not flushed: every step reads {w.kv_bytes() / 1e9:.2f} GB of KV, "
+               f"{w.kv_bytes() / L2_BYTES:.0f}x the {L2_BYTES >> 20} MiB L2"}
+    if cfg == 4:
+        d["l2"] = ("not flushed: the 32 shared prefix blocks (4 MB) are read by all 256 "
+                   "sequences in every step and stay in L2; value counts logical bytes")
+        d["unique_kv_bytes"] = unique_kv_bytes(w)
+    return d
+
+
+def unique_kv_bytes(w: synth.Workload) -> int:
+    """KV bytes of distinct (physical block, slot) rows the batch attends to."""
+    rows = set()
+    bs = w.block_size
+    for s in range(w.num_seqs):
+        L = int(w.context_lens[s])
+        for j in range((L + bs - 1) // bs):
+            rows.add((int(w.block_tables[s, j]), min(bs, L - j * bs)))
+    per_row = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+    used = {}
+    for b, n in rows:
+        used[b] = max(used.get(b, 0), n)
+    return sum(used.values()) * per_row
+
+
+# ------------------------------------------------------------------------------------------
+# measurement helpers
+# ------------------------------------------------------------------------------------------
+
+def hbm_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "samples": len(rows), "reasons": reasons}
+
+
+def traffic_for(w_name: str) -> float | None:
+    entry = MEASURED_TRAFFIC.get(w_name)
+    if not entry:
+        return None
+    import hashlib
+
+    src = os.path.join(ROOT, "paged_kv_cache_315_gb300", "csrc", "decode.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return float(entry["bytes"]) if entry.get("decode_cu_sha") == digest else None
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import paged_kv_cache_315_gb300 as pkv
+
+    pkv.load()
+    cfg = args.config
+    w = bench_workload(cfg)
+    part = w.partition_size if args.partition < 0 else args.partition
+    t = synth.to_torch(w, dev)
+    if cfg == 4:
+        # state: copy-on-write copies, then every suffix token
+        pkv.kv_copy_blocks(t["k_cache"], t["copy_pairs"])
+        pkv.kv_copy_blocks(t["v_cache"], t["copy_pairs"])
+        pkv.kv_cache_write(synth.storage_to_torch(w.info["setup_k"], "bf16", dev),
+                           synth.storage_to_torch(w.info["setup_v"], "bf16", dev),
+                           t["k_cache"], t["v_cache"],
+                           torch.from_numpy(w.info["setup_slots"]).to(dev))
+    out = torch.empty_like(t["q"])
+    B = w.num_seqs
+    ws = pkv.workspace_for(dev, pkv.paged_attn_decode_workspace_size(
+        B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.max_blocks_per_seq, part))
+    has_pairs = "copy_pairs" in t
+
+    def step(inp, ev=None):
+        if has_pairs:
+            pkv.kv_copy_blocks(t["k_cache"], inp["copy_pairs"])
+            pkv.kv_copy_blocks(t["v_cache"], inp["copy_pairs"])
+        pkv.kv_cache_write(inp["k_new"], inp["v_new"], t["k_cache"], t["v_cache"],
+                           inp["slot_mapping"])
+        if ev is not None:
+            ev[0].record()
+        pkv.paged_attn_decode(out, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
+                              inp["context_lens"], w.scale, partition_size=part, workspace=ws)
+        if ev is not None:
+            ev[1].record()
+
+    launches_per_step = (2 if has_pairs else 0) + 1 + 1
+    assert pkv.pkv_device_error() == 0
+    for _ in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    if pkv.pkv_device_error() != 0:
+        raise RuntimeError("device error bits set during warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    t0.record()
+    for i in range(args.steps):
+        step(t, evs[i])
+    t1.record()
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if pkv.pkv_device_error() != 0:
+        raise RuntimeError("device error bits set during the timed steps")
+    if world > 1:
+        m = torch.tensor([elapsed_ms, decode_ms], device=dev)
+        dist.all_reduce(m, op=dist.ReduceOp.MAX)
+        elapsed_ms, decode_ms = float(m[0]), float(m[1])
+
+    # end to end: per-step inputs from pinned host memory, result read back every step
+    e2e = None
+    if not args.no_e2e:
+        names = ["q", "block_tables", "context_lens", "k_new", "v_new", "slot_mapping"]
+        if has_pairs:
+            names.append("copy_pairs")
+        host = {n: t[n].cpu().pin_memory() for n in names}
+        dev_in = {n: torch.empty_like(t[n]) for n in names}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(h.numel() * h.element_size() for h in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+        stream = torch.cuda.current_stream()
+
+        def e2e_step():
+            for n in names:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            step(dev_in)
+            out_h.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        barrier()
+        s0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        barrier()
+        e2e_s = time.perf_counter() - s0
+        if world > 1:
+            m = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+            dist.all_reduce(m, op=dist.ReduceOp.MAX)
+            e2e_s = float(m[0])
+        e2e = {"value": round(w.kv_bytes() * args.steps * world / e2e_s / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_s * 1e3 / args.steps, 4),
+               "path": "pinned host inputs -> cudaMemcpyAsync -> C-ABI calls -> output to "
+                       "pinned host, stream synchronised every step"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = hbm_peak()
+    ab = algorithmic_bytes(w)
+    ms = elapsed_ms / args.steps
+    value = w.kv_bytes() * args.steps * world / (elapsed_ms / 1e3) / 1e9
+    achieved = ab["total"] / (decode_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
+        "config": describe(w, cfg, part),
+        "hbm_frac": round(value / peak, 4),
+        "queries_per_s": round(B * world / (ms / 1e3), 1),
+        "query_heads_per_s": round(B * w.num_q_heads * world / (ms / 1e3), 1),
+        "decode_ms": round(decode_ms, 5),
+        "roofline": {"kernel": "paged_attn_decode (decode_tc_kernel)", "bound": "hbm",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": ab,
+                     "traffic": traffic_for(w.name)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and reference arm)
+# ------------------------------------------------------------------------------------------
+
+def _oracle_seq(w, s):
+    import oracle
+
+    return oracle.paged_decode(w.q[s:s + 1], w.k_cache, w.v_cache, w.block_tables[s:s + 1],
+                               w.context_lens[s:s + 1], w.scale, w.dtype)
+
+
+def seq_kv_bytes(w, s) -> int:
+    return int(w.context_lens[s]) * 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+
+
+def cpu_baseline(w, seconds: float) -> dict:
+    """The fp64 oracle, as it stands, over sequences of the batch until ``seconds`` pass."""
+    import oracle
+
+    oracle.build()
+    done_bytes, done_seqs = 0, 0
+    s0 = time.perf_counter()
+    while True:
+        s = done_seqs % w.num_seqs
+        _oracle_seq(w, s)
+        done_bytes += seq_kv_bytes(w, s)
+        done_seqs += 1
+        el = time.perf_counter() - s0
+        if el >= seconds or done_seqs >= 4 * w.num_seqs:
+            break
+    return {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{done_seqs} sequences of the batch (all query heads each) in {el:.1f} s; "
+                      f"fp64 C oracle, OpenMP over (sequence, query head)"}
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    w = bench_workload(args.config)
+    part = w.partition_size if args.partition < 0 else args.partition
+    order = list(range(w.num_seqs))
+    for i in range(args.warmup):
+        _oracle_seq(w, order[i % len(order)])
+    done_bytes = 0
+    s0 = time.perf_counter()
+    for i in range(args.steps):
+        s = order[i % len(order)]
+        _oracle_seq(w, s)
+        done_bytes += seq_kv_bytes(w, s)
+    el = time.perf_counter() - s0
+    value = done_bytes / el / 1e9
+    cores = oracle.max_threads()
+    ms = el * 1e3 / args.steps
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
+        "config": describe(w, args.config, part),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "one sequence of the batch (all its query heads) per step, "
+                                   "cycling through the batch; fp64 C oracle, OpenMP"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

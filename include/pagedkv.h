@@ -1,0 +1,185 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv: paged KV-cache decode attention for GB300 (sm_103a).
+ *
+ * Three operations make up the data-parallel hot path of PagedAttention:
+ *
+ *   paged_attn_decode  single-token decode attention whose keys and values are gathered
+ *                      from fixed-size, non-contiguous physical KV blocks through a
+ *                      per-sequence block table (with a split-context variant for long
+ *                      contexts, merged by log-sum-exp);
+ *   kv_cache_write     writes each new token's key/value rows into the cache slot its
+ *                      slot mapping names;
+ *   kv_copy_blocks     copies whole physical blocks (copy-on-write of a shared block).
+ *
+ * Common conventions
+ *   - Every pointer argument is caller-owned DEVICE memory of the current CUDA device,
+ *     except where stated.  The library keeps no pointer after a call returns and
+ *     allocates no device memory.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Return codes report argument and launch errors only.
+ *   - Tensors are dense and row-major (C order).
+ *   - Cache layout: k_cache and v_cache are separate tensors of shape
+ *         [num_blocks, block_size, num_kv_heads, head_dim]
+ *     so token slot `slot` (= physical_block * block_size + offset) is row `slot` of the
+ *     cache seen as [num_blocks * block_size, num_kv_heads, head_dim].  This follows the
+ *     kernel sketch on the "Paged Attention" page (section "Paged Attention's Approach"),
+ *     whose cache is [num_blocks, block_size, hidden] indexed
+ *     [physical_block, in_block, head].
+ *   - Data errors found on the device (a block id, slot or pair id out of range, a
+ *     context length outside the block table) never trap: the offending unit is
+ *     skipped or clamped, a bit is set in the library's device error word, and
+ *     pkv_device_error() reports it.
+ *
+ * Element types: PKV_F32, PKV_BF16, PKV_F16.  Accumulation is always fp32.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle; binary-compatible with cudaStream_t / CUstream. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
+
+/* Return codes (host side). */
+#define PKV_OK 0
+#define PKV_EINVAL (-1)      /* null pointer, bad size, misaligned pointer, Hq % Hkv != 0 */
+#define PKV_ENOMEM (-2)      /* workspace smaller than paged_attn_decode_workspace_size() */
+#define PKV_ECUDA (-3)       /* the CUDA runtime reported an error while launching */
+#define PKV_EUNSUPPORTED (-4)/* head_dim / block_size / dtype combination not implemented */
+
+/* Device error bits (OR-ed together, reported by pkv_device_error). */
+#define PKV_DERR_BLOCK_ID 1u /* a live block-table entry outside [0, num_blocks) */
+#define PKV_DERR_SLOT 2u     /* a slot >= num_blocks * block_size */
+#define PKV_DERR_PAIR 4u     /* a copy pair naming a block outside [0, num_blocks) */
+#define PKV_DERR_CONTEXT 8u  /* context_len < 0 or > max_blocks_per_seq * block_size */
+#define PKV_DERR_TIMEOUT 16u /* a pipeline wait gave up after ~1 s (the call's output is void) */
+
+/*
+ * paged_attn_decode -- one decode query token per sequence attends to that sequence's
+ * cached keys and values, read block by block through its block table.
+ *
+ * What it computes ("PagedAttention: how vLLM manages the KV cache", section
+ * "PagedAttention changes addressing inside attention": the attention computation is
+ * unchanged, only the addressing of the cache differs).  For sequence s with
+ * L = context_lens[s], query head h and G = num_q_heads / num_kv_heads, the query reads
+ * KV head g = h / G (consecutive groups; "Grouped-query attention can reduce the
+ * KV-head term", same page, section "Keep the tensor formula beside the allocator
+ * model").  Logical position p (0 <= p < L) lives in physical block
+ * block_tables[s][p / block_size] at offset p % block_size ("Why vLLM Uses
+ * PagedAttention", section "Split the KV cache into 16-token blocks").  Then
+ *     out[s][h] = sum_p softmax_p( scale * <q[s][h], K_p> ) * V_p.
+ * L = 0 gives a zero output row.  Block-table entries past ceil(L / block_size) and
+ * cache slots past L are never read.
+ *
+ * The query heads of one KV head are processed together, so every cached byte is read
+ * from memory once.  Contexts longer than `partition_size` tokens are split into
+ * partitions whose partial results (running max, sum of exponentials, unnormalised
+ * output) are merged by log-sum-exp inside the same launch; the result equals the
+ * single-pass one up to rounding order.
+ *
+ * Arguments
+ *   out          [num_seqs, num_q_heads, head_dim], element type `dtype` (written).
+ *   q            [num_seqs, num_q_heads, head_dim], `dtype`.
+ *   k_cache,
+ *   v_cache      [num_blocks, block_size, num_kv_heads, head_dim], `dtype`; 16-byte aligned.
+ *   block_tables int32 [num_seqs, max_blocks_per_seq]; physical block ids.
+ *   context_lens int32 [num_seqs]; tokens attended per sequence (0 allowed).
+ *   scale        multiplies q.k before the softmax (typically 1/sqrt(head_dim)).
+ *   partition_size  tokens per split-context partition: 0 picks the library default
+ *                (512), otherwise a positive multiple of block_size.
+ *   workspace    device scratch of at least paged_attn_decode_workspace_size() bytes
+ *                (may be NULL when that size is 0), 16-byte aligned.  Its contents need
+ *                not be initialised: each call clears the part it needs (an asynchronous
+ *                memset on `stream`) before its kernel runs.  Calls that may run
+ *                concurrently must not share a workspace.
+ *   stream       CUDA stream to launch on.
+ * Supported: head_dim in {32, 64, 128, 256} (fp32 and fp16/bf16); the tensor-core path
+ * serves fp16/bf16 with head_dim 64 or 128, block_size 16, 32 or 64 and at most 16
+ * query heads per KV head; other shapes use the CUDA-core path.
+ * Returns PKV_OK, PKV_EINVAL, PKV_ENOMEM, PKV_EUNSUPPORTED or PKV_ECUDA.
+ */
+int paged_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int max_blocks_per_seq, int num_blocks, float scale, pkv_dtype dtype,
+                      int partition_size, void* workspace, size_t workspace_bytes,
+                      pkv_stream_t stream);
+
+/*
+ * Bytes of workspace paged_attn_decode needs for these sizes (0 when no sequence can
+ * span more than one partition).  Pure host function; no CUDA call.
+ */
+size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_blocks_per_seq,
+                                        int partition_size);
+
+/*
+ * kv_cache_write -- store new tokens' keys and values in their cache slots
+ * (the reshape-and-cache step).
+ *
+ * Blocks fill left to right as tokens are generated ("Why vLLM Uses PagedAttention",
+ * section "Split the KV cache into 16-token blocks"; "PagedAttention: how vLLM manages
+ * the KV cache", section "Walk one request through the allocator"): the caller's block
+ * manager picks each token's slot, slot = physical_block * block_size + offset, and
+ * this call copies the token's rows there:
+ *     k_cache[slot / block_size][slot % block_size][:][:] = k[i][:][:]   (same for v)
+ * A negative slot marks padding and is skipped.  A slot >= num_blocks * block_size is
+ * skipped and sets PKV_DERR_SLOT.  Two tokens naming the same slot in one call leave
+ * that slot undefined.  The copy is bit-exact.
+ *
+ *   k, v          [num_tokens, num_kv_heads, head_dim], `dtype`.
+ *   k_cache,
+ *   v_cache       [num_blocks, block_size, num_kv_heads, head_dim], `dtype` (written).
+ *   slot_mapping  int64 [num_tokens].
+ * Returns PKV_OK, PKV_EINVAL or PKV_ECUDA.  num_tokens = 0 is a no-op.
+ */
+int kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
+                   const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                   int block_size, int num_blocks, pkv_dtype dtype, pkv_stream_t stream);
+
+/*
+ * kv_copy_blocks -- copy whole physical blocks of one cache tensor, for copy-on-write.
+ *
+ * "PagedAttention: how vLLM manages the KV cache", section "Copy-on-write makes shared
+ * prefixes practical": when a branch must modify a shared last block, the manager
+ * allocates a new block and copies only that block.  For each pair i,
+ *     cache[dst_i] = cache[src_i]          (block_bytes bytes, bit-exact)
+ * with (src_i, dst_i) = (src_dst_pairs[2i], src_dst_pairs[2i+1]).  src == dst is a no-op.
+ * The destinations must be distinct and disjoint from the sources of the same call
+ * (otherwise the result is undefined).  A pair naming an id outside [0, num_blocks) is
+ * skipped and sets PKV_DERR_PAIR.  Call once for the key cache and once for the value
+ * cache.
+ *
+ *   cache          [num_blocks] blocks of block_bytes bytes each (written).
+ *   src_dst_pairs  int64 [num_pairs, 2], device memory.
+ *   block_bytes    bytes per block = block_size * num_kv_heads * head_dim * element size.
+ * Returns PKV_OK, PKV_EINVAL or PKV_ECUDA.  num_pairs = 0 is a no-op.
+ */
+int kv_copy_blocks(void* cache, const int64_t* src_dst_pairs, int num_pairs, size_t block_bytes,
+                   int num_blocks, pkv_stream_t stream);
+
+/*
+ * Synchronise `stream`, then return and clear the device error bits (PKV_DERR_*) that
+ * kernels of this library set on the current device since the last call.  Returns a
+ * negative PKV_ECUDA if the synchronisation itself failed.
+ */
+int pkv_device_error(pkv_stream_t stream);
+
+/* Static description of a return code or device error bit. */
+const char* pkv_strerror(int code);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,205 @@
+"""ctypes binding of libpagedkv (argument marshalling only).
+
+Every function passes device pointers of torch tensors, their sizes and the current
+CUDA stream to the C entry point of the same name; all the work happens in the
+library's CUDA kernels.  There is no fallback: if the library is not built, or a
+tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+PKV_F32, PKV_BF16, PKV_F16 = 0, 1, 2
+_DTYPES = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.float16: PKV_F16}
+
+PKV_DERR_BLOCK_ID = 1
+PKV_DERR_SLOT = 2
+PKV_DERR_PAIR = 4
+PKV_DERR_CONTEXT = 8
+PKV_DERR_TIMEOUT = 16
+
+_lock = threading.Lock()
+_lib = None
+_workspaces: dict = {}
+
+
+class PagedKVError(RuntimeError):
+    """A libpagedkv entry point returned an error code."""
+
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {pkv_strerror(code)} (code {code})")
+        self.code = code
+
+
+def load() -> ctypes.CDLL:
+    """Load libpagedkv.so from the package's build folder (raises if absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libpagedkv.so is not built ({LIB_PATH}); run "
+                "`python -m paged_kv_cache_315_gb300.build` first")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+        lib.paged_attn_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                          f32, i32, i32, P, sz, P]
+        lib.paged_attn_decode.restype = i32
+        lib.paged_attn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        lib.paged_attn_decode_workspace_size.restype = sz
+        lib.kv_cache_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
+        lib.kv_cache_write.restype = i32
+        lib.kv_copy_blocks.argtypes = [P, P, i32, sz, i32, P]
+        lib.kv_copy_blocks.restype = i32
+        lib.pkv_device_error.argtypes = [P]
+        lib.pkv_device_error.restype = i32
+        lib.pkv_strerror.argtypes = [i32]
+        lib.pkv_strerror.restype = ctypes.c_char_p
+        lib.pkv_version.argtypes = []
+        lib.pkv_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _cuda(name: str, t: torch.Tensor) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported element type {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != 0:
+        raise PagedKVError(fn, rc)
+
+
+def pkv_strerror(code: int) -> str:
+    return load().pkv_strerror(int(code)).decode()
+
+
+def pkv_version() -> int:
+    return int(load().pkv_version())
+
+
+def pkv_device_error(stream=None) -> int:
+    """Synchronise the stream; return and clear the device error bits (PKV_DERR_*)."""
+    rc = load().pkv_device_error(_stream(stream))
+    if rc < 0:
+        raise PagedKVError("pkv_device_error", rc)
+    return rc
+
+
+def paged_attn_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                     head_dim: int, block_size: int, max_blocks_per_seq: int,
+                                     partition_size: int = 0) -> int:
+    return int(load().paged_attn_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads,
+                                                       head_dim, block_size, max_blocks_per_seq,
+                                                       partition_size))
+
+
+def workspace_for(device, nbytes: int) -> torch.Tensor | None:
+    """A byte buffer of at least ``nbytes`` on ``device``, reused across calls.
+
+    The library clears what it needs in the workspace at every call, so one buffer
+    serves every call made on one stream, whatever the shapes.
+    """
+    if nbytes == 0:
+        return None
+    key = torch.device(device)
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=key)
+        _workspaces[key] = buf
+    return buf
+
+
+def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: float, partition_size: int = 0,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode attention over the paged cache; writes and returns ``out`` [B, Hq, D].
+
+    ``q``/``out`` [B, Hq, D]; ``k_cache``/``v_cache`` [NB, bs, Hkv, D];
+    ``block_tables`` int32 [B, MB]; ``context_lens`` int32 [B].
+    """
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if not (q.dtype == out.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q, out and the caches must share one element type")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_tables must be [B, MB] and context_lens [B]")
+    MB = block_tables.shape[1]
+    need = paged_attn_decode_workspace_size(B, Hq, Hkv, D, bs, MB, partition_size)
+    if workspace is None:
+        workspace = workspace_for(q.device, need)
+    ws_ptr = _cuda("workspace", workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().paged_attn_decode(
+        _cuda("out", out), _cuda("q", q), _cuda("k_cache", k_cache), _cuda("v_cache", v_cache),
+        _cuda("block_tables", block_tables), _cuda("context_lens", context_lens), B, Hq, Hkv, D,
+        bs, MB, NB, float(scale), _dtype(q), int(partition_size), ws_ptr, ws_bytes,
+        _stream(stream))
+    _check("paged_attn_decode", rc)
+    return out
+
+
+def kv_cache_write(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write token rows ``k[i]``/``v[i]`` [N, Hkv, D] into cache slot ``slot_mapping[i]``."""
+    NB, bs, Hkv, D = k_cache.shape
+    N = k.shape[0]
+    if tuple(k.shape) != (N, Hkv, D) or tuple(v.shape) != (N, Hkv, D):
+        raise ValueError("k and v must be [N, Hkv, D] matching the cache")
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must have the same shape")
+    if not (k.dtype == v.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("tokens and caches must share one element type")
+    if slot_mapping.dtype != torch.int64 or tuple(slot_mapping.shape) != (N,):
+        raise TypeError("slot_mapping must be int64 [N]")
+    if N == 0:
+        return
+    rc = load().kv_cache_write(_cuda("k", k), _cuda("v", v), _cuda("k_cache", k_cache),
+                               _cuda("v_cache", v_cache), _cuda("slot_mapping", slot_mapping), N,
+                               Hkv, D, bs, NB, _dtype(k), _stream(stream))
+    _check("kv_cache_write", rc)
+
+
+def kv_copy_blocks(cache: torch.Tensor, src_dst_pairs: torch.Tensor, stream=None) -> None:
+    """Copy whole blocks ``cache[src] -> cache[dst]`` for each row of ``src_dst_pairs`` [P, 2]."""
+    if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or \
+            src_dst_pairs.shape[1] != 2:
+        raise TypeError("src_dst_pairs must be int64 [P, 2]")
+    P = src_dst_pairs.shape[0]
+    if P == 0:
+        return
+    NB = cache.shape[0]
+    block_bytes = cache[0].numel() * cache.element_size()
+    rc = load().kv_copy_blocks(_cuda("cache", cache), _cuda("src_dst_pairs", src_dst_pairs), P,
+                               block_bytes, NB, _stream(stream))
+    _check("kv_copy_blocks", rc)

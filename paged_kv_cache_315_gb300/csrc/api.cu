@@ -1,0 +1,160 @@
+// api.cu -- the extern "C" entry points of libpagedkv: argument validation, dispatch to
+// the kernel launchers, and the device error word.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <mutex>
+
+#include "internal.h"
+#include "pagedkv.h"
+
+namespace pkv {
+namespace {
+
+// Data errors found by kernels (PKV_DERR_* bits); one word per device.
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+
+// Device address of this device's error word (host code may not take it directly).
+unsigned* error_word() {
+  static unsigned* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned*>(p);
+  }
+  return addr[dev];
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+bool valid_dtype(pkv_dtype d) { return d == PKV_F32 || d == PKV_BF16 || d == PKV_F16; }
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int paged_attn_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int max_blocks_per_seq, int num_blocks, float scale, pkv_dtype dtype,
+                      int partition_size, void* workspace, size_t workspace_bytes,
+                      pkv_stream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || !valid_dtype(dtype))
+    return PKV_EINVAL;
+  if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
+  if (static_cast<long long>(num_blocks) * block_size >= INT_MAX) return PKV_EINVAL;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size >= INT_MAX) return PKV_EINVAL;
+  const int ptok = resolve_partition_tokens(partition_size, block_size);
+  if (ptok < 0) return PKV_EINVAL;
+  if (!decode_supported(dtype, head_dim, block_size)) return PKV_EUNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_EINVAL;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return PKV_EINVAL;
+  if (workspace && !aligned(workspace, 16)) return PKV_EINVAL;
+  unsigned* err = error_word();
+  if (!err) return PKV_ECUDA;
+  DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.partition_tokens = ptok;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err = err;
+  return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_blocks_per_seq,
+                                        int partition_size) {
+  (void)num_kv_heads;
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0)
+    return 0;
+  const int ptok = resolve_partition_tokens(partition_size, block_size);
+  if (ptok < 0) return 0;
+  return workspace_layout(num_seqs, num_q_heads, head_dim, block_size, max_blocks_per_seq, ptok)
+      .total;
+}
+
+int kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
+                   const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                   int block_size, int num_blocks, pkv_dtype dtype, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || !valid_dtype(dtype))
+    return PKV_EINVAL;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_EINVAL;
+  if (!aligned(slot_mapping, 8)) return PKV_EINVAL;
+  unsigned* err = error_word();
+  if (!err) return PKV_ECUDA;
+  const size_t row_bytes = static_cast<size_t>(num_kv_heads) * head_dim * dtype_size(dtype);
+  const long long rows = static_cast<long long>(num_blocks) * block_size;
+  return launch_kv_cache_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, rows,
+                               err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kv_copy_blocks(void* cache, const int64_t* src_dst_pairs, int num_pairs, size_t block_bytes,
+                   int num_blocks, pkv_stream_t stream) {
+  if (num_pairs < 0 || num_blocks <= 0 || block_bytes == 0) return PKV_EINVAL;
+  if (num_pairs == 0) return PKV_OK;
+  if (!cache || !src_dst_pairs || !aligned(src_dst_pairs, 8)) return PKV_EINVAL;
+  unsigned* err = error_word();
+  if (!err) return PKV_ECUDA;
+  return launch_kv_copy_blocks(cache, src_dst_pairs, num_pairs, block_bytes, num_blocks, err,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pkv_device_error(pkv_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ECUDA;
+  unsigned bits = 0;
+  if (cudaMemcpyFromSymbol(&bits, g_error_word, sizeof bits) != cudaSuccess) return PKV_ECUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess) return PKV_ECUDA;
+  return static_cast<int>(bits);
+}
+
+const char* pkv_strerror(int code) {
+  switch (code) {
+    case PKV_OK: return "success";
+    case PKV_EINVAL: return "invalid argument";
+    case PKV_ENOMEM: return "workspace too small";
+    case PKV_ECUDA: return "CUDA runtime error";
+    case PKV_EUNSUPPORTED: return "unsupported head_dim / block_size / dtype combination";
+    case static_cast<int>(PKV_DERR_BLOCK_ID): return "device: block id out of range";
+    case static_cast<int>(PKV_DERR_SLOT): return "device: slot out of range";
+    case static_cast<int>(PKV_DERR_PAIR): return "device: copy pair id out of range";
+    case static_cast<int>(PKV_DERR_CONTEXT): return "device: context length outside the block table";
+    case static_cast<int>(PKV_DERR_TIMEOUT): return "device: pipeline wait timed out";
+    default: return "unknown code";
+  }
+}
+
+int pkv_version(void) { return 0x000100; }
+
+}  // extern "C"

@@ -1,0 +1,136 @@
+// cache_ops.cu -- slot-mapped writes of new tokens and whole-block copies (sm_103a).
+//
+// Both are pure byte movement, bound by HBM bandwidth: each thread moves 16-byte vectors
+// (narrower only when a size or pointer is not 16-byte aligned), grid-stride, with the
+// grid sized to a multiple of the SM count.
+#include <algorithm>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// k_cache row `slot` <- k row i (and the same for v); vec_per_row vectors of type V per row.
+template <typename V>
+__global__ void __launch_bounds__(kThreads)
+    kv_write_kernel(const V* __restrict__ k, const V* __restrict__ v, V* __restrict__ kc,
+                    V* __restrict__ vc, const int64_t* __restrict__ slots, long long num_tokens,
+                    long long vec_per_row, long long num_rows, unsigned* err) {
+  const long long total = num_tokens * vec_per_row;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const long long t = i / vec_per_row;
+    const long long col = i - t * vec_per_row;
+    const long long slot = __ldg(&slots[t]);
+    if (slot < 0) continue;  // padding
+    if (slot >= num_rows) {
+      if (col == 0) raise_error(err, PKV_DERR_SLOT);
+      continue;
+    }
+    const V kv = __ldg(&k[i]);
+    const V vv = __ldg(&v[i]);
+    kc[slot * vec_per_row + col] = kv;
+    vc[slot * vec_per_row + col] = vv;
+  }
+}
+
+// cache block dst <- cache block src for every pair; blockIdx.y strides over pairs.
+template <typename V>
+__global__ void __launch_bounds__(kThreads)
+    kv_copy_kernel(V* cache, const int64_t* __restrict__ pairs, int num_pairs,
+                   long long vec_per_block, long long num_blocks, unsigned* err) {
+  for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
+    const long long src = __ldg(&pairs[2LL * pi]);
+    const long long dst = __ldg(&pairs[2LL * pi + 1]);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(err, PKV_DERR_PAIR);
+      continue;
+    }
+    if (src == dst) continue;
+    const V* s = cache + src * vec_per_block;
+    V* d = cache + dst * vec_per_block;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+         i < vec_per_block; i += stride)
+      d[i] = s[i];
+  }
+}
+
+// Widest vector (16, 8, 4, 2 or 1 bytes) dividing `bytes` and every pointer's address.
+int vector_bytes(size_t bytes, std::initializer_list<const void*> ptrs) {
+  for (int w : {16, 8, 4, 2}) {
+    bool ok = bytes % w == 0;
+    for (const void* p : ptrs) ok = ok && (reinterpret_cast<uintptr_t>(p) % w == 0);
+    if (ok) return w;
+  }
+  return 1;
+}
+
+template <typename V>
+int write_with(const void* k, const void* v, void* kc, void* vc, const int64_t* slots,
+               int num_tokens, size_t row_bytes, long long num_rows, unsigned* err,
+               cudaStream_t stream) {
+  const long long vpr = static_cast<long long>(row_bytes / sizeof(V));
+  const long long total = static_cast<long long>(num_tokens) * vpr;
+  const long long want = (total + kThreads - 1) / kThreads;
+  const int grid = static_cast<int>(std::max(1LL, std::min(want, 8LL * sm_count())));
+  kv_write_kernel<V><<<grid, kThreads, 0, stream>>>(
+      static_cast<const V*>(k), static_cast<const V*>(v), static_cast<V*>(kc), static_cast<V*>(vc),
+      slots, num_tokens, vpr, num_rows, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+template <typename V>
+int copy_with(void* cache, const int64_t* pairs, int num_pairs, size_t block_bytes,
+              int num_blocks, unsigned* err, cudaStream_t stream) {
+  const long long vpb = static_cast<long long>(block_bytes / sizeof(V));
+  // enough CTAs per pair that each thread moves about four vectors, capped so that all
+  // pairs together fill the GPU a few times over
+  const long long per_pair = std::max(1LL, (vpb + 4LL * kThreads - 1) / (4LL * kThreads));
+  const int gy = std::min(num_pairs, 65535);
+  const int gx = static_cast<int>(std::min(per_pair, 1024LL));
+  kv_copy_kernel<V><<<dim3(gx, gy), kThreads, 0, stream>>>(static_cast<V*>(cache), pairs,
+                                                           num_pairs, vpb, num_blocks, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace
+
+int launch_kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, size_t row_bytes,
+                          long long num_rows, unsigned* err, cudaStream_t stream) {
+  if (num_tokens == 0) return PKV_OK;
+  switch (vector_bytes(row_bytes, {k, v, k_cache, v_cache})) {
+    case 16: return write_with<uint4>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, num_rows, err, stream);
+    case 8: return write_with<uint2>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, num_rows, err, stream);
+    case 4: return write_with<uint32_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, num_rows, err, stream);
+    case 2: return write_with<uint16_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, num_rows, err, stream);
+    default: return write_with<uint8_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, num_rows, err, stream);
+  }
+}
+
+int launch_kv_copy_blocks(void* cache, const int64_t* pairs, int num_pairs, size_t block_bytes,
+                          int num_blocks, unsigned* err, cudaStream_t stream) {
+  if (num_pairs == 0) return PKV_OK;
+  switch (vector_bytes(block_bytes, {cache})) {
+    case 16: return copy_with<uint4>(cache, pairs, num_pairs, block_bytes, num_blocks, err, stream);
+    case 8: return copy_with<uint2>(cache, pairs, num_pairs, block_bytes, num_blocks, err, stream);
+    case 4: return copy_with<uint32_t>(cache, pairs, num_pairs, block_bytes, num_blocks, err, stream);
+    case 2: return copy_with<uint16_t>(cache, pairs, num_pairs, block_bytes, num_blocks, err, stream);
+    default: return copy_with<uint8_t>(cache, pairs, num_pairs, block_bytes, num_blocks, err, stream);
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,772 @@
+// decode.cu -- paged single-token decode attention for sm_103a.
+//
+// Work unit: one CTA per (sequence s, KV head g, query-head chunk c, context partition p).
+// The CTA walks the partition's logical blocks j, resolves each through the block table
+// to a physical block, and streams that block's K and V tiles ([block_size, head_dim]
+// each, one KV head) into shared memory with TMA.  All query heads of KV head g that
+// fall in chunk c are scored against every staged tile, so each cached byte leaves HBM
+// once per call ("PagedAttention: how vLLM manages the KV cache": attention itself is
+// unchanged, the kernel reads keys and values block by block through the request's
+// logical-to-physical mapping).
+//
+// Pipeline: four consumer warps; logical block j goes to warp j % 4 and to ring stage
+// j % S (S a multiple of 4, so every stage belongs to one warp).  Thread 0 issues the
+// first S tile loads; afterwards the warp that finishes a stage refills it with the
+// block S positions further on.  Each stage has one mbarrier (TMA transaction bytes);
+// every wait gives up after ~1 s and sets PKV_DERR_TIMEOUT.
+//
+// Math per warp, per block: an online softmax in base 2 (scores pre-multiplied by
+// scale*log2(e)): running max m, running sum l, unnormalised output o, rescaled by
+// 2^(m_old - m_new) whenever the max grows.  The four warps' (m, l, o) are merged in
+// shared memory at the end.  Contexts longer than one partition leave (m, l, o) per
+// partition in the workspace; the last CTA of a (s, g, c) to finish -- found with an
+// atomic ticket (cleared before the launch), no waiting -- merges them by log-sum-exp and
+// writes the output.
+//
+// Tensor-core path (fp16/bf16, head_dim 64/128, block_size 16/32/64): S = Q.K^T and
+// O += P.V with mma.sync m16n8k16 (fp32 accumulate); up to 16 query heads form the M
+// rows.  Tiles arrive with the 128-byte TMA swizzle so ldmatrix reads are
+// bank-conflict free.  CUDA-core path: everything else (fp32, other head sizes).
+#include <algorithm>
+#include <climits>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kTcHeads = 16;    // query heads per CTA on the tensor-core path
+constexpr int kSimtHeads = 8;   // ... on the CUDA-core path
+constexpr int kMaxStageSet = 4; // stages per warp, at most
+constexpr int kMaxParts = 1024; // partitions per sequence, at most
+
+struct Params {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws_o;
+  float* ws_ml;
+  unsigned* ws_cnt;
+  unsigned* err;
+  int num_q_heads, num_kv_heads, group, head_chunk, num_chunks;
+  int max_blocks_per_seq, num_blocks, block_size;
+  int partition_blocks, max_parts, stages;
+  int tile_bytes;   // bytes of one K (or V) tile
+  int tile_stride;  // tile_bytes rounded up to 1024: V tile offset inside a stage
+  int stage_bytes, box_bytes, box_cols, boxes, ring_bytes;
+  float scale_log2;
+};
+
+struct Work {
+  int s, g, c, p;
+  int np;         // partitions of this sequence
+  int blk0;       // first logical block of the partition
+  int nblk;       // blocks in the partition
+  int tok_valid;  // tokens of the partition that are live
+  int h0, hc;     // first query head and number of heads of this CTA
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Decode blockIdx into a work unit.  Returns false when the CTA has nothing to do (after
+// writing zeros for an empty context).
+template <typename T>
+__device__ bool decode_work(const Params& P, int D, Work& w) {
+  long long bid = blockIdx.x;
+  w.c = static_cast<int>(bid % P.num_chunks);
+  bid /= P.num_chunks;
+  w.g = static_cast<int>(bid % P.num_kv_heads);
+  bid /= P.num_kv_heads;
+  w.p = static_cast<int>(bid % P.max_parts);
+  w.s = static_cast<int>(bid / P.max_parts);
+  w.h0 = w.g * P.group + w.c * P.head_chunk;
+  w.hc = min(P.head_chunk, P.group - w.c * P.head_chunk);
+  int L = P.context_lens[w.s];
+  const int Lmax = P.max_blocks_per_seq * P.block_size;
+  if (L < 0 || L > Lmax) {
+    if (threadIdx.x == 0 && w.p == 0 && w.g == 0 && w.c == 0) raise_error(P.err, PKV_DERR_CONTEXT);
+    L = L < 0 ? 0 : Lmax;
+  }
+  const int ptok = P.partition_blocks * P.block_size;
+  w.np = (L + ptok - 1) / ptok;
+  if (L == 0) {
+    if (w.p == 0) {
+      T* out = static_cast<T*>(P.out) + (static_cast<size_t>(w.s) * P.num_q_heads + w.h0) * D;
+      for (int i = threadIdx.x; i < w.hc * D; i += kThreads) out[i] = from_f32<T>(0.f);
+    }
+    return false;
+  }
+  if (w.p >= w.np) return false;
+  w.blk0 = w.p * P.partition_blocks;
+  w.tok_valid = min(ptok, L - w.p * ptok);
+  w.nblk = (w.tok_valid + P.block_size - 1) / P.block_size;
+  return true;
+}
+
+struct Smem {
+  uint8_t* ring;
+  uint64_t* bars;
+  int* ycoord;
+  int* flags;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw, const Params& P) {
+  Smem s;
+  const uint32_t a = smem_addr(raw);
+  s.ring = raw + ((1024u - (a & 1023u)) & 1023u);
+  s.bars = reinterpret_cast<uint64_t*>(s.ring + P.ring_bytes);
+  s.ycoord = reinterpret_cast<int*>(s.bars + P.stages);
+  s.flags = s.ycoord + P.partition_blocks;
+  return s;
+}
+
+// Resolve the partition's block ids to TMA row coordinates (invalid ids point past the
+// tensor, so their tiles load as zeros), initialise the stage barriers and issue the
+// first S tile loads.
+__device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, const Smem& sm,
+                                               const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                               int x0);
+
+__device__ __forceinline__ void issue_tile(const Params& P, const Smem& sm, const CUtensorMap* kmap,
+                                           const CUtensorMap* vmap, int j, int x0) {
+  const int st = j % P.stages;
+  const uint32_t bar = smem_addr(&sm.bars[st]);
+  const uint32_t kdst = smem_addr(sm.ring + st * P.stage_bytes);
+  const uint32_t vdst = kdst + P.tile_stride;
+  const int y = sm.ycoord[j];
+  mbar_arrive_expect_tx(bar, 2u * P.tile_bytes);
+  for (int b = 0; b < P.boxes; ++b) {
+    tma_load_2d(kdst + b * P.box_bytes, kmap, bar, x0 + b * P.box_cols, y);
+    tma_load_2d(vdst + b * P.box_bytes, vmap, bar, x0 + b * P.box_cols, y);
+  }
+}
+
+__device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, const Smem& sm,
+                                               const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                               int x0) {
+  const int tid = threadIdx.x;
+  const int32_t* bt = P.block_tables + static_cast<size_t>(w.s) * P.max_blocks_per_seq + w.blk0;
+  for (int j = tid; j < w.nblk; j += kThreads) {
+    int id = bt[j];
+    if (id < 0 || id >= P.num_blocks) {
+      raise_error(P.err, PKV_DERR_BLOCK_ID);
+      id = P.num_blocks;
+    }
+    sm.ycoord[j] = id * P.block_size;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < P.stages; ++i) mbar_init(smem_addr(&sm.bars[i]), 1);
+    sm.flags[0] = 0;
+    sm.flags[1] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    tma_prefetch_desc(kmap);
+    tma_prefetch_desc(vmap);
+    const int first = min(P.stages, w.nblk);
+    for (int j = 0; j < first; ++j) issue_tile(P, sm, kmap, vmap, j, x0);
+  }
+}
+
+// After a timed-out wait on block j: wait (bounded) for this warp's loads still in flight.
+__device__ __forceinline__ void drain_after_timeout(const Params& P, const Work& w, const Smem& sm,
+                                                    int j) {
+  const int end = min(w.nblk, j + P.stages);
+  for (int jj = j; jj < end; jj += kWarps)
+    mbar_wait_bounded(smem_addr(&sm.bars[jj % P.stages]), (jj / P.stages) & 1);
+}
+
+// Merge the four warps' (m, l, o) of each query head; write the output (one partition)
+// or this partition's partials, and let the last partition CTA merge all partials.
+// O_s: [kWarps][HC][D] floats, ml_s: [kWarps][HC][2] (m in log2 units, l), wts: [HC][np].
+template <typename T>
+__device__ void finish(const Params& P, const Work& w, int D, int HC, const float* O_s,
+                       const float* ml_s, float* wts, int* flags) {
+  const int tid = threadIdx.x;
+  const int n = w.hc * D;
+  const bool split = w.np > 1;
+  T* out = static_cast<T*>(P.out);
+  for (int i = tid; i < n; i += kThreads) {
+    const int r = i / D, d = i - r * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int wi = 0; wi < kWarps; ++wi) M = fmaxf(M, ml_s[(wi * HC + r) * 2]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < kWarps; ++wi) {
+      const float mw = ml_s[(wi * HC + r) * 2];
+      const float cw = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      num += cw * O_s[(wi * HC + r) * D + d];
+      den += cw * ml_s[(wi * HC + r) * 2 + 1];
+    }
+    const size_t row = static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r;
+    if (!split) {
+      out[row * D + d] = from_f32<T>(num / den);
+    } else {
+      const size_t idx = row * P.max_parts + w.p;
+      P.ws_o[idx * D + d] = num;
+      if (d == 0) {
+        P.ws_ml[idx * 2] = M;
+        P.ws_ml[idx * 2 + 1] = den;
+      }
+    }
+  }
+  if (!split) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    unsigned* cnt =
+        P.ws_cnt + (static_cast<size_t>(w.s) * P.num_kv_heads + w.g) * P.num_chunks + w.c;
+    const unsigned prev = atomicAdd(cnt, 1u);
+    flags[1] = prev == static_cast<unsigned>(w.np - 1);
+  }
+  __syncthreads();
+  if (!flags[1]) return;
+  __threadfence();
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int r = warp; r < w.hc; r += kWarps) {
+    const size_t base = (static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r) * P.max_parts;
+    float M = -INFINITY;
+    for (int p = lane; p < w.np; p += 32) M = fmaxf(M, __ldcg(&P.ws_ml[(base + p) * 2]));
+    M = warp_max(M);
+    float den = 0.f;
+    for (int p = lane; p < w.np; p += 32) {
+      const float e = exp2f(__ldcg(&P.ws_ml[(base + p) * 2]) - M);
+      wts[r * w.np + p] = e;
+      den += e * __ldcg(&P.ws_ml[(base + p) * 2 + 1]);
+    }
+    den = warp_sum(den);
+    const float inv = 1.f / den;
+    for (int p = lane; p < w.np; p += 32) wts[r * w.np + p] *= inv;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) {
+    const int r = i / D, d = i - r * D;
+    const size_t row = static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r;
+    const size_t base = row * P.max_parts;
+    float acc = 0.f;
+    for (int p = 0; p < w.np; ++p) acc += wts[r * w.np + p] * __ldcg(&P.ws_o[(base + p) * D + d]);
+    out[row * D + d] = from_f32<T>(acc);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// tensor-core path
+// ------------------------------------------------------------------------------------------
+
+// Byte offset of (row r, column d) in a tile stored as 64-column boxes of 128-byte rows
+// with the TMA 128-byte swizzle (16-byte chunk index XOR row % 8); d a multiple of 8.
+template <int BS>
+__device__ __forceinline__ uint32_t swz(int r, int d) {
+  return static_cast<uint32_t>((d >> 6) * (BS * 128) + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4));
+}
+
+template <typename T, int D, int BS>
+__device__ __forceinline__ void tc_block(uint32_t kb, uint32_t vb, const uint32_t (&qa)[D / 16][4],
+                                         float (&o)[D / 8][4], float (&m)[2], float (&l)[2],
+                                         int valid, float scale_log2, int lane) {
+  constexpr int NT = BS / 8;  // 8-token column tiles of S
+  float sc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  const int mi = lane >> 3;
+  // S = Q . K^T : A = Q fragments (16 heads x 16 dims), B = K rows via ldmatrix.
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int r = nt * 8 + (lane & 7);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; kk += 2) {
+      const int d = (kk + (mi >> 1)) * 16 + (mi & 1) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kb + swz<BS>(r, d), b0, b1, b2, b3);
+      Mma<T>::run(sc[nt], qa[kk], b0, b1);
+      Mma<T>::run(sc[nt], qa[kk + 1], b2, b3);
+    }
+  }
+  // scale into log2 units, mask tokens past the context, row maxima over the quad
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int tok = nt * 8 + (lane & 3) * 2 + (c & 1);
+      const float v = sc[nt][c] * scale_log2;
+      sc[nt][c] = tok < valid ? v : -INFINITY;
+    }
+    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+  const float a0 = exp2f(m[0] - mn0), a1 = exp2f(m[1] - mn1);
+  m[0] = mn0;
+  m[1] = mn1;
+  // P = 2^(S - m) rounded to the operand type; the row sums use the rounded weights
+  uint32_t pa[BS / 16][4];
+  float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint32_t lo = Mma<T>::pack(exp2f(sc[nt][0] - mn0), exp2f(sc[nt][1] - mn0));
+    const uint32_t hi = Mma<T>::pack(exp2f(sc[nt][2] - mn1), exp2f(sc[nt][3] - mn1));
+    const float2 flo = Mma<T>::unpack(lo), fhi = Mma<T>::unpack(hi);
+    rs0 += flo.x + flo.y;
+    rs1 += fhi.x + fhi.y;
+    pa[nt >> 1][(nt & 1) * 2 + 0] = lo;
+    pa[nt >> 1][(nt & 1) * 2 + 1] = hi;
+  }
+  l[0] = l[0] * a0 + rs0;
+  l[1] = l[1] * a1 + rs1;
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) {
+    o[nd][0] *= a0;
+    o[nd][1] *= a0;
+    o[nd][2] *= a1;
+    o[nd][3] *= a1;
+  }
+  // O += P . V : B = V rows via transposing ldmatrix.
+#pragma unroll
+  for (int kt = 0; kt < BS / 16; ++kt) {
+    const int r = kt * 16 + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int nd = 0; nd < D / 8; nd += 2) {
+      const int d = (nd + (mi >> 1)) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_trans(vb + swz<BS>(r, d), b0, b1, b2, b3);
+      Mma<T>::run(o[nd], pa[kt], b0, b1);
+      Mma<T>::run(o[nd + 1], pa[kt], b2, b3);
+    }
+  }
+}
+
+// Zero V rows [valid, BS) of a swizzled tile: masked tokens get weight 0, but 0 * NaN
+// from stale slots would still poison the product.
+template <int D, int BS>
+__device__ __forceinline__ void zero_tail_rows(uint8_t* vtile, int valid, int lane) {
+  constexpr int kBoxes = D / 64;
+  const int rows = BS - valid;
+  const int n = kBoxes * rows * 8;  // 16-byte chunks
+  for (int i = lane; i < n; i += 32) {
+    const int b = i / (rows * 8);
+    const int rem = i - b * rows * 8;
+    const int r = valid + rem / 8;
+    const int ch = rem & 7;
+    *reinterpret_cast<uint4*>(vtile + b * BS * 128 + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(kThreads)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap, const Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  Work w;
+  if (!decode_work<T>(P, D, w)) return;
+  const Smem sm = carve(smem_raw, P);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int x0 = w.g * D;
+  pipeline_start(P, w, sm, &kmap, &vmap, x0);
+
+  // Q fragments (A operand, rows = query heads of this CTA, zero past hc)
+  uint32_t qa[D / 16][4];
+  {
+    const T* qs = static_cast<const T*>(P.q) + (static_cast<size_t>(w.s) * P.num_q_heads + w.h0) * D;
+    const int r0 = lane >> 2, cq = (lane & 3) * 2;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int c0 = kk * 16 + cq;
+      qa[kk][0] = r0 < w.hc ? __ldg(reinterpret_cast<const uint32_t*>(qs + r0 * D + c0)) : 0u;
+      qa[kk][1] = r0 + 8 < w.hc ? __ldg(reinterpret_cast<const uint32_t*>(qs + (r0 + 8) * D + c0)) : 0u;
+      qa[kk][2] = r0 < w.hc ? __ldg(reinterpret_cast<const uint32_t*>(qs + r0 * D + c0 + 8)) : 0u;
+      qa[kk][3] =
+          r0 + 8 < w.hc ? __ldg(reinterpret_cast<const uint32_t*>(qs + (r0 + 8) * D + c0 + 8)) : 0u;
+    }
+  }
+  float o[D / 8][4];
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+  for (int j = warp; j < w.nblk; j += kWarps) {
+    const int st = j % P.stages;
+    if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (j / P.stages) & 1)) {
+      if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
+      drain_after_timeout(P, w, sm, j);
+      break;
+    }
+    uint8_t* ktile = sm.ring + st * P.stage_bytes;
+    uint8_t* vtile = ktile + P.tile_stride;
+    const int valid = min(BS, w.tok_valid - j * BS);
+    if (valid < BS) {
+      zero_tail_rows<D, BS>(vtile, valid, lane);
+      __syncwarp();
+    }
+    tc_block<T, D, BS>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
+    __syncwarp();
+    if (lane == 0 && j + P.stages < w.nblk) {
+      fence_proxy_async_smem();
+      issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0);
+    }
+  }
+
+  __syncthreads();  // all stages consumed: the ring becomes the merge buffer
+  float* O_s = reinterpret_cast<float*>(sm.ring);
+  float* ml_s = O_s + kWarps * kTcHeads * D;
+  float* wts = ml_s + kWarps * kTcHeads * 2;
+  {
+    const int r0 = lane >> 2;
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      const int col = nd * 8 + (lane & 3) * 2;
+      if (r0 < w.hc)
+        *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0) * D + col]) = make_float2(o[nd][0], o[nd][1]);
+      if (r0 + 8 < w.hc)
+        *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0 + 8) * D + col]) =
+            make_float2(o[nd][2], o[nd][3]);
+    }
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+    if ((lane & 3) == 0) {
+      if (r0 < w.hc) {
+        ml_s[(warp * kTcHeads + r0) * 2] = m[0];
+        ml_s[(warp * kTcHeads + r0) * 2 + 1] = l[0];
+      }
+      if (r0 + 8 < w.hc) {
+        ml_s[(warp * kTcHeads + r0 + 8) * 2] = m[1];
+        ml_s[(warp * kTcHeads + r0 + 8) * 2 + 1] = l[1];
+      }
+    }
+  }
+  __syncthreads();
+  finish<T>(P, w, D, kTcHeads, O_s, ml_s, wts, sm.flags);
+}
+
+// ------------------------------------------------------------------------------------------
+// CUDA-core path
+// ------------------------------------------------------------------------------------------
+
+template <typename T, int E>
+__global__ void __launch_bounds__(kThreads)
+    decode_simt_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const Params P) {
+  constexpr int D = 32 * E;
+  constexpr int HC = kSimtHeads;
+  extern __shared__ uint8_t smem_raw[];
+  Work w;
+  if (!decode_work<T>(P, D, w)) return;
+  const Smem sm = carve(smem_raw, P);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int x0 = w.g * D;
+  const int BS = P.block_size;
+  pipeline_start(P, w, sm, &kmap, &vmap, x0);
+
+  float qr[HC][E];
+  {
+    const T* qs = static_cast<const T*>(P.q) + (static_cast<size_t>(w.s) * P.num_q_heads + w.h0) * D;
+#pragma unroll
+    for (int h = 0; h < HC; ++h)
+#pragma unroll
+      for (int e = 0; e < E; ++e) qr[h][e] = h < w.hc ? to_f32(qs[h * D + lane * E + e]) : 0.f;
+  }
+  float acc[HC][E], m[HC], l[HC];
+#pragma unroll
+  for (int h = 0; h < HC; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[h][e] = 0.f;
+  }
+
+  for (int j = warp; j < w.nblk; j += kWarps) {
+    const int st = j % P.stages;
+    if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (j / P.stages) & 1)) {
+      if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
+      drain_after_timeout(P, w, sm, j);
+      break;
+    }
+    const T* kt = reinterpret_cast<const T*>(sm.ring + st * P.stage_bytes);
+    const T* vt = reinterpret_cast<const T*>(sm.ring + st * P.stage_bytes + P.tile_stride);
+    const int valid = min(BS, w.tok_valid - j * BS);
+    for (int t = 0; t < valid; ++t) {
+      float kf[E], vf[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        kf[e] = to_f32(kt[t * D + lane * E + e]);
+        vf[e] = to_f32(vt[t * D + lane * E + e]);
+      }
+#pragma unroll
+      for (int h = 0; h < HC; ++h) {
+        if (h < w.hc) {
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) dot = fmaf(qr[h][e], kf[e], dot);
+          const float sl = warp_sum(dot) * P.scale_log2;
+          const float mn = fmaxf(m[h], sl);
+          const float a = exp2f(m[h] - mn);
+          const float pr = exp2f(sl - mn);
+          l[h] = l[h] * a + pr;
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[h][e] = fmaf(pr, vf[e], acc[h][e] * a);
+          m[h] = mn;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && j + P.stages < w.nblk) {
+      fence_proxy_async_smem();
+      issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0);
+    }
+  }
+
+  __syncthreads();
+  float* O_s = reinterpret_cast<float*>(sm.ring);
+  float* ml_s = O_s + kWarps * HC * D;
+  float* wts = ml_s + kWarps * HC * 2;
+#pragma unroll
+  for (int h = 0; h < HC; ++h) {
+    if (h < w.hc) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) O_s[(warp * HC + h) * D + lane * E + e] = acc[h][e];
+      if (lane == 0) {
+        ml_s[(warp * HC + h) * 2] = m[h];
+        ml_s[(warp * HC + h) * 2 + 1] = l[h];
+      }
+    }
+  }
+  __syncthreads();
+  finish<T>(P, w, D, HC, O_s, ml_s, wts, sm.flags);
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// The cache seen as a 2-D tensor: x = num_kv_heads * head_dim elements, y = cache rows.
+bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dt, int Hkv, int D,
+                    long long rows, int box_cols, int box_rows, bool swizzle) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const CUtensorMapDataType t = dt == PKV_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hkv) * D, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hkv) * D * dtype_size(dt)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
+
+template <typename T>
+KernelFn tc_kernel_for(int D, int BS) {
+  if (D == 64) {
+    if (BS == 16) return decode_tc_kernel<T, 64, 16>;
+    if (BS == 32) return decode_tc_kernel<T, 64, 32>;
+    if (BS == 64) return decode_tc_kernel<T, 64, 64>;
+  } else if (D == 128) {
+    if (BS == 16) return decode_tc_kernel<T, 128, 16>;
+    if (BS == 32) return decode_tc_kernel<T, 128, 32>;
+    if (BS == 64) return decode_tc_kernel<T, 128, 64>;
+  }
+  return nullptr;
+}
+
+template <typename T>
+KernelFn simt_kernel_for(int D) {
+  switch (D) {
+    case 32: return decode_simt_kernel<T, 1>;
+    case 64: return decode_simt_kernel<T, 2>;
+    case 128: return decode_simt_kernel<T, 4>;
+    case 256: return decode_simt_kernel<T, 8>;
+    default: return nullptr;
+  }
+}
+
+KernelFn kernel_for(pkv_dtype dt, int D, int BS, bool tc) {
+  if (tc) {
+    if (dt == PKV_BF16) return tc_kernel_for<__nv_bfloat16>(D, BS);
+    if (dt == PKV_F16) return tc_kernel_for<__half>(D, BS);
+    return nullptr;
+  }
+  if (dt == PKV_F32) return simt_kernel_for<float>(D);
+  if (dt == PKV_BF16) return simt_kernel_for<__nv_bfloat16>(D);
+  return simt_kernel_for<__half>(D);
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Geometry {
+  int stages, tile_bytes, tile_stride, stage_bytes, ring_bytes, smem_bytes;
+};
+
+Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, int max_parts) {
+  Geometry g{};
+  g.tile_bytes = BS * D * static_cast<int>(dtype_size(dt));
+  g.tile_stride = static_cast<int>(align_up(g.tile_bytes, 1024));
+  g.stage_bytes = 2 * g.tile_stride;
+  const int per_warp = std::max(1, std::min(kMaxStageSet, 16384 / g.stage_bytes));
+  g.stages = kWarps * per_warp;
+  const int HC = tc ? kTcHeads : kSimtHeads;
+  const size_t epi = (static_cast<size_t>(kWarps) * HC * D + kWarps * HC * 2 +
+                      static_cast<size_t>(HC) * max_parts) * sizeof(float);
+  g.ring_bytes = static_cast<int>(
+      align_up(std::max(static_cast<size_t>(g.stages) * g.stage_bytes, epi), 1024));
+  g.smem_bytes = 1024 + g.ring_bytes + 8 * g.stages + 4 * partition_blocks + 16;
+  return g;
+}
+
+constexpr int kMaxSmem = 227 * 1024;
+
+}  // namespace
+
+size_t dtype_size(pkv_dtype dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+int resolve_partition_tokens(int partition_size, int block_size) {
+  if (block_size <= 0) return -1;
+  if (partition_size == 0) {
+    const int t = (kDefaultPartitionTokens / block_size) * block_size;
+    return t > 0 ? t : block_size;
+  }
+  if (partition_size < 0 || partition_size % block_size != 0) return -1;
+  if (partition_size / block_size > kMaxPartitionBlocks) return -1;
+  return partition_size;
+}
+
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int block_size,
+                                 int max_blocks_per_seq, int partition_tokens) {
+  WorkspaceLayout w{};
+  const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+  w.max_parts = static_cast<int>(std::max(1LL, (max_ctx + partition_tokens - 1) / partition_tokens));
+  if (w.max_parts <= 1) return w;
+  const size_t units = static_cast<size_t>(num_seqs) * num_q_heads * w.max_parts;
+  w.o_offset = 0;
+  w.ml_offset = align_up(units * head_dim * sizeof(float), 256);
+  w.cnt_offset = w.ml_offset + align_up(units * 2 * sizeof(float), 256);
+  w.total = w.cnt_offset + align_up(static_cast<size_t>(num_seqs) * num_q_heads * sizeof(unsigned), 256);
+  return w;
+}
+
+bool decode_uses_tensor_cores(pkv_dtype dtype, int head_dim, int block_size) {
+  return (dtype == PKV_BF16 || dtype == PKV_F16) && (head_dim == 64 || head_dim == 128) &&
+         (block_size == 16 || block_size == 32 || block_size == 64);
+}
+
+bool decode_supported(pkv_dtype dtype, int head_dim, int block_size) {
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256) return false;
+  if (block_size < 1 || block_size > 256) return false;
+  const bool tc = decode_uses_tensor_cores(dtype, head_dim, block_size);
+  const Geometry g = geometry(dtype, head_dim, block_size, tc, 1, 1);
+  return g.smem_bytes <= kMaxSmem;
+}
+
+int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.num_seqs == 0) return PKV_OK;
+  const bool tc = decode_uses_tensor_cores(a.dtype, a.head_dim, a.block_size);
+  const int D = a.head_dim, BS = a.block_size;
+  const WorkspaceLayout wl = workspace_layout(a.num_seqs, a.num_q_heads, D, BS,
+                                              a.max_blocks_per_seq, a.partition_tokens);
+  if (wl.max_parts > kMaxParts) return PKV_EUNSUPPORTED;
+  if (wl.total > 0 && (a.workspace == nullptr || a.workspace_bytes < wl.total)) return PKV_ENOMEM;
+
+  Params P{};
+  P.out = a.out;
+  P.q = a.q;
+  P.block_tables = a.block_tables;
+  P.context_lens = a.context_lens;
+  P.err = a.err;
+  P.num_q_heads = a.num_q_heads;
+  P.num_kv_heads = a.num_kv_heads;
+  P.group = a.num_q_heads / a.num_kv_heads;
+  P.head_chunk = std::min(P.group, tc ? kTcHeads : kSimtHeads);
+  P.num_chunks = (P.group + P.head_chunk - 1) / P.head_chunk;
+  P.max_blocks_per_seq = a.max_blocks_per_seq;
+  P.num_blocks = a.num_blocks;
+  P.block_size = BS;
+  P.partition_blocks = a.partition_tokens / BS;
+  P.max_parts = wl.max_parts;
+  if (wl.total > 0) {
+    char* ws = static_cast<char*>(a.workspace);
+    P.ws_o = reinterpret_cast<float*>(ws + wl.o_offset);
+    P.ws_ml = reinterpret_cast<float*>(ws + wl.ml_offset);
+    P.ws_cnt = reinterpret_cast<unsigned*>(ws + wl.cnt_offset);
+  }
+  const Geometry g = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts);
+  if (g.smem_bytes > kMaxSmem) return PKV_EUNSUPPORTED;
+  P.stages = g.stages;
+  P.tile_bytes = g.tile_bytes;
+  P.tile_stride = g.tile_stride;
+  P.stage_bytes = g.stage_bytes;
+  P.ring_bytes = g.ring_bytes;
+  P.boxes = tc ? D / 64 : 1;
+  P.box_cols = tc ? 64 : D;
+  P.box_bytes = tc ? BS * 128 : g.tile_bytes;
+  P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+
+  const long long grid = static_cast<long long>(a.num_seqs) * wl.max_parts * a.num_kv_heads *
+                         P.num_chunks;
+  if (grid > INT_MAX) return PKV_EUNSUPPORTED;
+
+  CUtensorMap kmap, vmap;
+  const long long rows = static_cast<long long>(a.num_blocks) * BS;
+  if (!make_cache_map(&kmap, a.k_cache, a.dtype, a.num_kv_heads, D, rows, P.box_cols, BS, tc) ||
+      !make_cache_map(&vmap, a.v_cache, a.dtype, a.num_kv_heads, D, rows, P.box_cols, BS, tc))
+    return PKV_ECUDA;
+
+  KernelFn fn = kernel_for(a.dtype, D, BS, tc);
+  if (!fn) return PKV_EUNSUPPORTED;
+  // the partition tickets count up from zero in every call
+  if (wl.total > 0 &&
+      cudaMemsetAsync(P.ws_cnt, 0, wl.total - wl.cnt_offset, stream) != cudaSuccess)
+    return PKV_ECUDA;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes) != cudaSuccess)
+    return PKV_ECUDA;
+  fn<<<static_cast<unsigned>(grid), kThreads, g.smem_bytes, stream>>>(kmap, vmap, P);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+}  // namespace pkv

@@ -1,0 +1,60 @@
+// internal.h -- host-side interfaces between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+constexpr int kDefaultPartitionTokens = 512;
+constexpr int kMaxPartitionBlocks = 2048;
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
+  int max_blocks_per_seq, num_blocks;
+  float scale;
+  pkv_dtype dtype;
+  int partition_tokens;  // resolved: a positive multiple of block_size
+  void* workspace;
+  size_t workspace_bytes;
+  unsigned* err;  // device error word
+};
+
+// Resolved partition size in tokens, or -1 if `partition_size` is not acceptable.
+int resolve_partition_tokens(int partition_size, int block_size);
+
+// Workspace layout shared by the size query and the launcher.
+struct WorkspaceLayout {
+  size_t o_offset, ml_offset, cnt_offset, total;
+  int max_parts;
+};
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int block_size,
+                                 int max_blocks_per_seq, int partition_tokens);
+
+// Whether the tensor-core path serves this shape (otherwise the CUDA-core path does).
+bool decode_uses_tensor_cores(pkv_dtype dtype, int head_dim, int block_size);
+// Whether any decode path serves this shape.
+bool decode_supported(pkv_dtype dtype, int head_dim, int block_size);
+
+int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+int launch_kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, size_t row_bytes,
+                          long long num_rows, unsigned* err, cudaStream_t stream);
+
+int launch_kv_copy_blocks(void* cache, const int64_t* pairs, int num_pairs, size_t block_bytes,
+                          int num_blocks, unsigned* err, cudaStream_t stream);
+
+size_t dtype_size(pkv_dtype dtype);
+
+}  // namespace pkv

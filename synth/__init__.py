@@ -393,17 +393,22 @@ def shared_prefix_workload(*, seed: int, num_seqs: int = 256, prefix_tokens: int
     return w
 
 
+def storage_to_torch(a: np.ndarray, dtype: str, device):
+    """A torch tensor on ``device`` holding the elements stored in ``a``."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype != "f32":
+        t = t.view(torch.int16).view({"bf16": torch.bfloat16, "f16": torch.float16}[dtype])
+    return t.to(device)
+
+
 def to_torch(w: Workload, device):
     """Device copies of a workload's arrays, as a dict of torch tensors."""
     import torch
 
-    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.dtype]
-
     def elems(a):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        if w.dtype != "f32":
-            t = t.view(torch.int16).view(tdt)
-        return t.to(device)
+        return storage_to_torch(a, w.dtype, device)
 
     out = {
         "q": elems(w.q),

@@ -1,0 +1,88 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol the header
+declares, and its pure-host entry points and argument checks behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"#[^\n]*", "", text)
+        for m in re.finditer(r"^[A-Za-z_][\w \t\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M):
+            name = m.group(1)
+            if name not in ("if", "while", "for", "return", "sizeof"):
+                names.append(name)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_315_gb300 import build
+
+    path = build()
+    import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_three_operations():
+    names = _declared_functions()
+    for n in ("paged_attn_decode", "kv_cache_write", "kv_copy_blocks",
+              "paged_attn_decode_workspace_size", "pkv_device_error", "pkv_strerror"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_host_only_entry_points(lib):
+    import paged_kv_cache_315_gb300 as pkv
+
+    assert pkv.pkv_version() == 0x000100
+    assert pkv.pkv_strerror(-1) == "invalid argument"
+    # contexts that fit one partition need no workspace
+    assert pkv.paged_attn_decode_workspace_size(4, 4, 4, 64, 16, 7, 0) == 0
+    # 64 partitions of 512 tokens: o partials, (m, l) pairs and per-unit counters
+    n = pkv.paged_attn_decode_workspace_size(32, 32, 8, 128, 16, 2048, 512)
+    units = 32 * 32 * 64
+    assert n >= units * 128 * 4 + units * 2 * 4 + 32 * 32 * 4
+    assert n < units * 130 * 4 + 64 * 1024
+    # partition sizes must be multiples of the block size
+    assert pkv.paged_attn_decode_workspace_size(32, 32, 8, 128, 16, 2048, 100) == 0
+
+
+def test_argument_checks_return_before_any_cuda_call(lib):
+    """Invalid shapes are rejected on the host (these calls never touch a device)."""
+    null = ctypes.c_void_p(0)
+    f = lib.paged_attn_decode
+    f.restype = ctypes.c_int
+    args = lambda hq, hkv, d, bs, dt, part: (  # noqa: E731
+        null, null, null, null, null, null, ctypes.c_int(2), ctypes.c_int(hq), ctypes.c_int(hkv),
+        ctypes.c_int(d), ctypes.c_int(bs), ctypes.c_int(8), ctypes.c_int(16), ctypes.c_float(0.1),
+        ctypes.c_int(dt), ctypes.c_int(part), null, ctypes.c_size_t(0), null)
+    assert f(*args(6, 4, 128, 16, 1, 0)) == -1      # Hq % Hkv != 0
+    assert f(*args(8, 4, 128, 16, 7, 0)) == -1      # bad dtype
+    assert f(*args(8, 4, 128, 16, 1, 24)) == -1     # partition not a multiple of block_size
+    assert f(*args(8, 4, 96, 16, 1, 0)) == -4       # head_dim not served
+    assert f(*args(8, 4, 128, 16, 1, 0)) == -1      # null pointers
+    w = lib.kv_cache_write
+    w.restype = ctypes.c_int
+    assert w(null, null, null, null, null, ctypes.c_int(-1), 4, 128, 16, 16, 1, null) == -1
+    assert w(null, null, null, null, null, ctypes.c_int(0), 4, 128, 16, 16, 1, null) == 0
+    c = lib.kv_copy_blocks
+    c.restype = ctypes.c_int
+    assert c(null, null, ctypes.c_int(0), ctypes.c_size_t(64), 4, null) == 0
+    assert c(null, null, ctypes.c_int(3), ctypes.c_size_t(64), 4, null) == -1
