@@ -38,8 +38,15 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) per launch of the decode kernel, from one ncu capture per
-# workload, valid only for the kernel source whose hash is recorded beside it.
-MEASURED_TRAFFIC: dict = {}
+# workload and partition size, valid only for the kernel source whose hash is recorded
+# beside it (profiles/ holds the captures).
+MEASURED_TRAFFIC: dict = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each
+    "13b-mha-b64-bf16@2048": {"bytes": 1408906000 + 4161792, "decode_cu_sha": "13d0b5ae3ca7754a"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 964765696 + 8224512, "decode_cu_sha": "13d0b5ae3ca7754a"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328558848 + 4712704, "decode_cu_sha": "13d0b5ae3ca7754a"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4327292416 + 36300032, "decode_cu_sha": "13d0b5ae3ca7754a"},
+}
 
 
 def parse_args(argv=None):
@@ -98,7 +105,7 @@ def describe(w: synth.Workload, cfg: int, part: int) -> dict:
     pool = 2 * w.k_cache.nbytes
     d = {"workload": w.name, "recipe": synth.CONFIGS[cfg], "batch": w.num_seqs,
          "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-         "block_size": w.block_size, "partition_tokens": part if part > 0 else 512,
+         "block_size": w.block_size,
          "context_tokens": int(w.context_lens.sum()),
          "context_min_mean_max": [int(w.context_lens.min()), float(w.context_lens.mean()),
                                   int(w.context_lens.max())],
@@ -188,8 +195,8 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-def traffic_for(w_name: str) -> float | None:
-    entry = MEASURED_TRAFFIC.get(w_name)
+def traffic_for(w_name: str, part: int) -> float | None:
+    entry = MEASURED_TRAFFIC.get(f"{w_name}@{part}")
     if not entry:
         return None
     import hashlib
@@ -232,6 +239,8 @@ def run_ours(args) -> None:
                            torch.from_numpy(w.info["setup_slots"]).to(dev))
     out = torch.empty_like(t["q"])
     B = w.num_seqs
+    part = pkv.paged_attn_decode_partition_tokens(B, w.num_q_heads, w.num_kv_heads, w.block_size,
+                                                  w.max_blocks_per_seq, part)
     ws = pkv.workspace_for(dev, pkv.paged_attn_decode_workspace_size(
         B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.max_blocks_per_seq, part))
     has_pairs = "copy_pairs" in t
@@ -352,11 +361,12 @@ def run_ours(args) -> None:
         "queries_per_s": round(B * world / (ms / 1e3), 1),
         "query_heads_per_s": round(B * w.num_q_heads * world / (ms / 1e3), 1),
         "decode_ms": round(decode_ms, 5),
+        "partition_tokens": part,
         "roofline": {"kernel": "paged_attn_decode (decode_tc_kernel)", "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": ab,
-                     "traffic": traffic_for(w.name)},
+                     "traffic": traffic_for(w.name, part)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

@@ -75,8 +75,10 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
  * block_tables[s][p / block_size] at offset p % block_size ("Why vLLM Uses
  * PagedAttention", section "Split the KV cache into 16-token blocks").  Then
  *     out[s][h] = sum_p softmax_p( scale * <q[s][h], K_p> ) * V_p.
- * L = 0 gives a zero output row.  Block-table entries past ceil(L / block_size) and
- * cache slots past L are never read.
+ * L = 0 gives a zero output row.  The values of block-table entries past
+ * ceil(L / block_size) never matter (the kernel may load an entry of the row early,
+ * before it knows L, but never dereferences one past the context), and cache slots past
+ * L are never read.
  *
  * The query heads of one KV head are processed together, so every cached byte is read
  * from memory once.  Contexts longer than `partition_size` tokens are split into
@@ -92,8 +94,11 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
  *   block_tables int32 [num_seqs, max_blocks_per_seq]; physical block ids.
  *   context_lens int32 [num_seqs]; tokens attended per sequence (0 allowed).
  *   scale        multiplies q.k before the softmax (typically 1/sqrt(head_dim)).
- *   partition_size  tokens per split-context partition: 0 picks the library default
- *                (512), otherwise a positive multiple of block_size.
+ *   partition_size  tokens per split-context partition: a positive multiple of
+ *                block_size, or 0 for the library's choice -- the largest of 2048, 1024
+ *                and 512 tokens that still gives at least 2048 work units (sequences x
+ *                KV heads x partitions, every sequence counted at the block table's full
+ *                length).  paged_attn_decode_workspace_size makes the same choice.
  *   workspace    device scratch of at least paged_attn_decode_workspace_size() bytes
  *                (may be NULL when that size is 0), 16-byte aligned.  Its contents need
  *                not be initialised: each call clears the part it needs (an asynchronous
@@ -119,6 +124,15 @@ int paged_attn_decode(void* out, const void* q, const void* k_cache, const void*
 size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                         int head_dim, int block_size, int max_blocks_per_seq,
                                         int partition_size);
+
+/*
+ * The partition size (tokens) paged_attn_decode uses for these sizes and this
+ * `partition_size` argument (0 resolves to the library's choice), or PKV_EINVAL.  Pure
+ * host function; no CUDA call.
+ */
+int paged_attn_decode_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int block_size, int max_blocks_per_seq,
+                                       int partition_size);
 
 /*
  * kv_cache_write -- store new tokens' keys and values in their cache slots

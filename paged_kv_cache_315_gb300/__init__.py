@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     kv_copy_blocks,
     load,
     paged_attn_decode,
+    paged_attn_decode_partition_tokens,
     paged_attn_decode_workspace_size,
     pkv_device_error,
     pkv_strerror,

@@ -54,6 +54,8 @@ def load() -> ctypes.CDLL:
         lib.paged_attn_decode.restype = i32
         lib.paged_attn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         lib.paged_attn_decode_workspace_size.restype = sz
+        lib.paged_attn_decode_partition_tokens.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.paged_attn_decode_partition_tokens.restype = i32
         lib.kv_cache_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
         lib.kv_cache_write.restype = i32
         lib.kv_copy_blocks.argtypes = [P, P, i32, sz, i32, P]
@@ -117,6 +119,17 @@ def paged_attn_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_hea
     return int(load().paged_attn_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads,
                                                        head_dim, block_size, max_blocks_per_seq,
                                                        partition_size))
+
+
+def paged_attn_decode_partition_tokens(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                       block_size: int, max_blocks_per_seq: int,
+                                       partition_size: int = 0) -> int:
+    rc = int(load().paged_attn_decode_partition_tokens(num_seqs, num_q_heads, num_kv_heads,
+                                                        block_size, max_blocks_per_seq,
+                                                        partition_size))
+    if rc < 0:
+        raise PagedKVError("paged_attn_decode_partition_tokens", rc)
+    return rc
 
 
 def workspace_for(device, nbytes: int) -> torch.Tensor | None:

@@ -43,6 +43,7 @@ constexpr int kTcHeads = 16;    // query heads per CTA on the tensor-core path
 constexpr int kSimtHeads = 8;   // ... on the CUDA-core path
 constexpr int kMaxStageSet = 4; // stages per warp, at most
 constexpr int kMaxParts = 1024; // partitions per sequence, at most
+constexpr long long kMinUnits = 2048;  // work units the default partition size aims for
 
 struct Params {
   void* out;
@@ -53,7 +54,7 @@ struct Params {
   float* ws_ml;
   unsigned* ws_cnt;
   unsigned* err;
-  int num_q_heads, num_kv_heads, group, head_chunk, num_chunks;
+  int num_seqs, num_q_heads, num_kv_heads, group, head_chunk, num_chunks;
   int max_blocks_per_seq, num_blocks, block_size;
   int partition_blocks, max_parts, stages;
   int tile_bytes;   // bytes of one K (or V) tile
@@ -83,10 +84,14 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Decode blockIdx into a work unit.  Returns false when the CTA has nothing to do (after
-// writing zeros for an empty context).
+// Decode blockIdx into a work unit: (sequence, partition, KV head, head chunk) from
+// slowest to fastest, so the KV heads of one physical block are read by neighbouring
+// CTAs.  Returns false when the CTA has nothing to do (after writing zeros for an empty
+// context).  `spec_id` receives this thread's entry of the partition's block-table row,
+// loaded before the context length is known so that the two loads overlap (an entry past
+// the context is loaded but never used).
 template <typename T>
-__device__ bool decode_work(const Params& P, int D, Work& w) {
+__device__ bool decode_work(const Params& P, int D, Work& w, int& spec_id) {
   long long bid = blockIdx.x;
   w.c = static_cast<int>(bid % P.num_chunks);
   bid /= P.num_chunks;
@@ -96,6 +101,10 @@ __device__ bool decode_work(const Params& P, int D, Work& w) {
   w.s = static_cast<int>(bid / P.max_parts);
   w.h0 = w.g * P.group + w.c * P.head_chunk;
   w.hc = min(P.head_chunk, P.group - w.c * P.head_chunk);
+  const int jb = w.p * P.partition_blocks + static_cast<int>(threadIdx.x);
+  spec_id = (static_cast<int>(threadIdx.x) < P.partition_blocks && jb < P.max_blocks_per_seq)
+                ? __ldg(&P.block_tables[static_cast<size_t>(w.s) * P.max_blocks_per_seq + jb])
+                : -1;
   int L = P.context_lens[w.s];
   const int Lmax = P.max_blocks_per_seq * P.block_size;
   if (L < 0 || L > Lmax) {
@@ -140,7 +149,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const Params& P) {
 // first S tile loads.
 __device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, const Smem& sm,
                                                const CUtensorMap* kmap, const CUtensorMap* vmap,
-                                               int x0);
+                                               int x0, int spec_id);
 
 __device__ __forceinline__ void issue_tile(const Params& P, const Smem& sm, const CUtensorMap* kmap,
                                            const CUtensorMap* vmap, int j, int x0) {
@@ -158,11 +167,11 @@ __device__ __forceinline__ void issue_tile(const Params& P, const Smem& sm, cons
 
 __device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, const Smem& sm,
                                                const CUtensorMap* kmap, const CUtensorMap* vmap,
-                                               int x0) {
+                                               int x0, int spec_id) {
   const int tid = threadIdx.x;
   const int32_t* bt = P.block_tables + static_cast<size_t>(w.s) * P.max_blocks_per_seq + w.blk0;
   for (int j = tid; j < w.nblk; j += kThreads) {
-    int id = bt[j];
+    int id = j == tid ? spec_id : bt[j];
     if (id < 0 || id >= P.num_blocks) {
       raise_error(P.err, PKV_DERR_BLOCK_ID);
       id = P.num_blocks;
@@ -379,11 +388,12 @@ __global__ void __launch_bounds__(kThreads)
                      const __grid_constant__ CUtensorMap vmap, const Params P) {
   extern __shared__ uint8_t smem_raw[];
   Work w;
-  if (!decode_work<T>(P, D, w)) return;
+  int spec_id;
+  if (!decode_work<T>(P, D, w, spec_id)) return;
   const Smem sm = carve(smem_raw, P);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int x0 = w.g * D;
-  pipeline_start(P, w, sm, &kmap, &vmap, x0);
+  pipeline_start(P, w, sm, &kmap, &vmap, x0, spec_id);
 
   // Q fragments (A operand, rows = query heads of this CTA, zero past hc)
   uint32_t qa[D / 16][4];
@@ -417,14 +427,12 @@ __global__ void __launch_bounds__(kThreads)
     const int valid = min(BS, w.tok_valid - j * BS);
     if (valid < BS) {
       zero_tail_rows<D, BS>(vtile, valid, lane);
+      fence_proxy_async_smem();  // generic writes before the stage's next TMA fill
       __syncwarp();
     }
     tc_block<T, D, BS>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
     __syncwarp();
-    if (lane == 0 && j + P.stages < w.nblk) {
-      fence_proxy_async_smem();
-      issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0);
-    }
+    if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0);
   }
 
   __syncthreads();  // all stages consumed: the ring becomes the merge buffer
@@ -473,12 +481,13 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int HC = kSimtHeads;
   extern __shared__ uint8_t smem_raw[];
   Work w;
-  if (!decode_work<T>(P, D, w)) return;
+  int spec_id;
+  if (!decode_work<T>(P, D, w, spec_id)) return;
   const Smem sm = carve(smem_raw, P);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int x0 = w.g * D;
   const int BS = P.block_size;
-  pipeline_start(P, w, sm, &kmap, &vmap, x0);
+  pipeline_start(P, w, sm, &kmap, &vmap, x0, spec_id);
 
   float qr[HC][E];
   {
@@ -532,10 +541,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     __syncwarp();
-    if (lane == 0 && j + P.stages < w.nblk) {
-      fence_proxy_async_smem();
-      issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0);
-    }
+    if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0);
   }
 
   __syncthreads();
@@ -665,11 +671,24 @@ constexpr int kMaxSmem = 227 * 1024;
 
 size_t dtype_size(pkv_dtype dtype) { return dtype == PKV_F32 ? 4 : 2; }
 
-int resolve_partition_tokens(int partition_size, int block_size) {
+int resolve_partition_tokens(int partition_size, int block_size, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int max_blocks_per_seq) {
   if (block_size <= 0) return -1;
   if (partition_size == 0) {
-    const int t = (kDefaultPartitionTokens / block_size) * block_size;
-    return t > 0 ? t : block_size;
+    // The largest of 2048, 1024, 512 tokens that still leaves at least kMinUnits work
+    // units (sequence x KV head x 16-head chunk x partition, counting every sequence at
+    // the block table's full length); longer partitions amortise each CTA's start-up
+    // cost, shorter ones balance uneven contexts across the SMs.
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    const int group = num_kv_heads > 0 ? std::max(1, num_q_heads / num_kv_heads) : 1;
+    const long long heads = static_cast<long long>(std::max(0, num_seqs)) *
+                            std::max(1, num_kv_heads) * ((group + kTcHeads - 1) / kTcHeads);
+    int t = 0;
+    for (int cand : {2048, 1024, kDefaultPartitionTokens}) {
+      t = std::max(block_size, (cand / block_size) * block_size);
+      if (heads * ((max_ctx + t - 1) / t) >= kMinUnits) break;
+    }
+    return t;
   }
   if (partition_size < 0 || partition_size % block_size != 0) return -1;
   if (partition_size / block_size > kMaxPartitionBlocks) return -1;
@@ -718,6 +737,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   P.block_tables = a.block_tables;
   P.context_lens = a.context_lens;
   P.err = a.err;
+  P.num_seqs = a.num_seqs;
   P.num_q_heads = a.num_q_heads;
   P.num_kv_heads = a.num_kv_heads;
   P.group = a.num_q_heads / a.num_kv_heads;

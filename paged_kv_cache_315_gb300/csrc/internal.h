@@ -31,7 +31,9 @@ struct DecodeArgs {
 };
 
 // Resolved partition size in tokens, or -1 if `partition_size` is not acceptable.
-int resolve_partition_tokens(int partition_size, int block_size);
+// 0 selects a default from the batch's shape (pure host arithmetic).
+int resolve_partition_tokens(int partition_size, int block_size, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int max_blocks_per_seq);
 
 // Workspace layout shared by the size query and the launcher.
 struct WorkspaceLayout {

@@ -86,3 +86,24 @@ def test_argument_checks_return_before_any_cuda_call(lib):
     c.restype = ctypes.c_int
     assert c(null, null, ctypes.c_int(0), ctypes.c_size_t(64), 4, null) == 0
     assert c(null, null, ctypes.c_int(3), ctypes.c_size_t(64), 4, null) == -1
+
+
+def test_default_partition_size_follows_available_parallelism(lib):
+    import paged_kv_cache_315_gb300 as pkv
+
+    f = pkv.paged_attn_decode_partition_tokens
+    # 64 seqs x 40 KV heads already give 2560 units at 2048 tokens
+    assert f(64, 40, 40, 16, 128, 0) == 2048
+    # 128 seqs x 8 KV heads x 4 partitions of 2048 (8192-token tables)
+    assert f(128, 64, 8, 16, 512, 0) == 2048
+    # a small batch splits finer
+    assert f(4, 32, 8, 16, 2048, 0) == 512
+    assert f(128, 64, 8, 16, 128, 0) == 1024  # 1024 (seq, head) pairs x 2 partitions
+    # an explicit size is kept; block size 48 rounds the default down to a multiple
+    assert f(32, 32, 8, 16, 2048, 512) == 512
+    assert f(64, 40, 40, 48, 64, 0) % 48 == 0
+    with pytest.raises(pkv.PagedKVError):
+        f(32, 32, 8, 16, 2048, 100)
+    # the workspace query makes the same choice
+    assert pkv.paged_attn_decode_workspace_size(4, 32, 8, 128, 16, 2048, 0) == \
+        pkv.paged_attn_decode_workspace_size(4, 32, 8, 128, 16, 2048, 512)
