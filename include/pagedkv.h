@@ -53,6 +53,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
 #define PKV_ENOMEM (-2)      /* workspace smaller than paged_attn_decode_workspace_size() */
 #define PKV_ECUDA (-3)       /* the CUDA runtime reported an error while launching */
 #define PKV_EUNSUPPORTED (-4)/* head_dim / block_size / dtype combination not implemented */
+#define PKV_ESCRATCH (-5)    /* needs more scratch than paged_attn_decode_noalloc has */
 
 /* Device error bits (OR-ed together, reported by pkv_device_error). */
 #define PKV_DERR_BLOCK_ID 1u /* a live block-table entry outside [0, num_blocks) */
@@ -178,6 +179,36 @@ int kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
  */
 int kv_copy_blocks(void* cache, const int64_t* src_dst_pairs, int num_pairs, size_t block_bytes,
                    int num_blocks, pkv_stream_t stream);
+
+/*
+ * paged_attn_decode_noalloc -- paged_attn_decode for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call; it exists for users of this library.
+ * paged_attn_decode needs scratch memory (the `workspace`), which its caller allocates.
+ * Some callers cannot: a host program that owns the device's whole memory budget and
+ * passes the library nothing but the tensors of each call, or a hot path on which no
+ * allocation may happen.  This variant takes the same arguments minus the workspace and
+ * uses instead a scratch array compiled into the library: PKV_NOALLOC_SCRATCH_BYTES of
+ * device memory that every GPU which loads the library holds until the process exits.
+ * It never allocates (no cudaMalloc or cudaFree, no allocating library routine).
+ *
+ *   - A problem whose scratch (paged_attn_decode_workspace_size) exceeds
+ *     PKV_NOALLOC_SCRATCH_BYTES is rejected with PKV_ESCRATCH before any device work;
+ *     use paged_attn_decode with a workspace for it, or a larger partition_size.
+ *   - The first call on each device looks up the scratch array's device address (once,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array, and it keeps the last call's contents;
+ *     each call clears the counters it needs (a memset on `stream`) before its kernel.
+ *     Calls whose work can overlap on the GPU (different streams without ordering
+ *     between them) race on the array and give wrong results; order them.
+ * Otherwise it behaves exactly as paged_attn_decode, with the same return codes.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+int paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                              pkv_dtype dtype, int partition_size, pkv_stream_t stream);
 
 /*
  * Synchronise `stream`, then return and clear the device error bits (PKV_DERR_*) that

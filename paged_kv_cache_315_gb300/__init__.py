@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     PKV_DERR_PAIR,
     PKV_DERR_SLOT,
     PKV_DERR_TIMEOUT,
+    PKV_ESCRATCH,
     PKV_F16,
     PKV_F32,
     PagedKVError,
@@ -25,6 +26,7 @@ from ._binding import (  # noqa: F401
     kv_copy_blocks,
     load,
     paged_attn_decode,
+    paged_attn_decode_noalloc,
     paged_attn_decode_partition_tokens,
     paged_attn_decode_workspace_size,
     pkv_device_error,

@@ -23,6 +23,7 @@ PKV_DERR_SLOT = 2
 PKV_DERR_PAIR = 4
 PKV_DERR_CONTEXT = 8
 PKV_DERR_TIMEOUT = 16
+PKV_ESCRATCH = -5
 
 _lock = threading.Lock()
 _lib = None
@@ -56,6 +57,9 @@ def load() -> ctypes.CDLL:
         lib.paged_attn_decode_workspace_size.restype = sz
         lib.paged_attn_decode_partition_tokens.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.paged_attn_decode_partition_tokens.restype = i32
+        lib.paged_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32,
+                                                  i32, i32, f32, i32, i32, P]
+        lib.paged_attn_decode_noalloc.restype = i32
         lib.kv_cache_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
         lib.kv_cache_write.restype = i32
         lib.kv_copy_blocks.argtypes = [P, P, i32, sz, i32, P]
@@ -179,6 +183,33 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         bs, MB, NB, float(scale), _dtype(q), int(partition_size), ws_ptr, ws_bytes,
         _stream(stream))
     _check("paged_attn_decode", rc)
+    return out
+
+
+def paged_attn_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                              v_cache: torch.Tensor, block_tables: torch.Tensor,
+                              context_lens: torch.Tensor, scale: float, partition_size: int = 0,
+                              stream=None) -> torch.Tensor:
+    """``paged_attn_decode`` without a workspace: for callers that may not allocate.
+
+    The library's built-in scratch (``PKV_NOALLOC_SCRATCH_BYTES`` per device) stands in
+    for the workspace; calls that overlap on the GPU race on it.  Raises
+    ``PagedKVError`` (code -5) when the problem needs more scratch than that.
+    """
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if not (q.dtype == out.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q, out and the caches must share one element type")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    rc = load().paged_attn_decode_noalloc(
+        _cuda("out", out), _cuda("q", q), _cuda("k_cache", k_cache), _cuda("v_cache", v_cache),
+        _cuda("block_tables", block_tables), _cuda("context_lens", context_lens), B, Hq, Hkv, D,
+        bs, block_tables.shape[1], NB, float(scale), _dtype(q), int(partition_size),
+        _stream(stream))
+    _check("paged_attn_decode_noalloc", rc)
     return out
 
 
