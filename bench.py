@@ -206,6 +206,25 @@ def traffic_for(w_name: str, part: int) -> float | None:
     return float(entry["bytes"]) if entry.get("decode_cu_sha") == digest else None
 
 
+def max_over_ranks(values, world: int) -> list:
+    """Element-wise max of ``values`` over all ranks (the values themselves for one rank)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_gbs(bytes_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job GB/s of ``world`` replicas that each moved ``bytes_per_step`` per step."""
+    return bytes_per_step * steps * world / seconds / 1e9
+
+
 # ------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------
@@ -287,10 +306,7 @@ def run_ours(args) -> None:
     decode_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     if pkv.pkv_device_error() != 0:
         raise RuntimeError("device error bits set during the timed steps")
-    if world > 1:
-        m = torch.tensor([elapsed_ms, decode_ms], device=dev)
-        dist.all_reduce(m, op=dist.ReduceOp.MAX)
-        elapsed_ms, decode_ms = float(m[0]), float(m[1])
+    elapsed_ms, decode_ms = max_over_ranks([elapsed_ms, decode_ms], world)
 
     # end to end: per-step inputs from pinned host memory, result read back every step
     e2e = None
@@ -320,11 +336,8 @@ def run_ours(args) -> None:
             e2e_step()
         barrier()
         e2e_s = time.perf_counter() - s0
-        if world > 1:
-            m = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-            dist.all_reduce(m, op=dist.ReduceOp.MAX)
-            e2e_s = float(m[0])
-        e2e = {"value": round(w.kv_bytes() * args.steps * world / e2e_s / 1e9, 2), "unit": "GB/s",
+        (e2e_s,) = max_over_ranks([e2e_s], world)
+        e2e = {"value": round(replica_gbs(w.kv_bytes(), args.steps, world, e2e_s), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e2e_s * 1e3 / args.steps, 4),
                "path": "pinned host inputs -> cudaMemcpyAsync -> C-ABI calls -> output to "
@@ -341,7 +354,7 @@ def run_ours(args) -> None:
     peak, peak_kind = hbm_peak()
     ab = algorithmic_bytes(w)
     ms = elapsed_ms / args.steps
-    value = w.kv_bytes() * args.steps * world / (elapsed_ms / 1e3) / 1e9
+    value = replica_gbs(w.kv_bytes(), args.steps, world, elapsed_ms / 1e3)
     achieved = ab["total"] / (decode_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
