@@ -63,6 +63,10 @@ def parse_args(argv=None):
                    help="CPU time budget of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--op", choices=["decode", "swap"], default="decode",
+                   help="decode (default): the decode step; swap: block swaps device <-> host")
+    p.add_argument("--swap-blocks", type=int, default=4096,
+                   help="blocks per swap direction for --op swap")
     return p.parse_args(argv)
 
 
@@ -464,8 +468,82 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_swap(args) -> None:
+    """Swap out / swap in of scattered blocks between the device pool and pinned host memory.
+
+    The 70B-like GQA pool (16-token bf16 blocks, 8 KV heads: 32 KB per block per tensor);
+    `--swap-blocks` random blocks go out to a pinned host pool and back in, K and V each.
+    The reference ceiling is a contiguous cudaMemcpyAsync of the same bytes, each way.
+    """
+    import torch
+
+    import paged_kv_cache_315_gb300 as pkv
+
+    torch.cuda.set_device(0)
+    pkv.load()
+    w = synth.config_workload(3, with_writes=False)
+    t = synth.to_torch(w, "cuda")
+    n = min(args.swap_blocks, w.num_blocks)
+    rng = np.random.default_rng(synth.BASE_SEED + 50)
+    blocks = rng.choice(w.num_blocks, size=n, replace=False).astype(np.int64)
+    host_k = torch.empty((n,) + tuple(t["k_cache"].shape[1:]), dtype=t["k_cache"].dtype).pin_memory()
+    host_v = torch.empty_like(host_k).pin_memory()
+    out_pairs = torch.from_numpy(np.stack([blocks, np.arange(n)], axis=1)).cuda()
+    in_pairs = torch.from_numpy(np.stack([np.arange(n), blocks], axis=1)).cuda()
+    block_bytes = t["k_cache"][0].numel() * t["k_cache"].element_size()
+    moved = 2 * n * block_bytes  # K and V, one direction
+
+    def swap_out():
+        pkv.kv_swap_blocks(host_k, t["k_cache"], out_pairs)
+        pkv.kv_swap_blocks(host_v, t["v_cache"], out_pairs)
+
+    def swap_in():
+        pkv.kv_swap_blocks(t["k_cache"], host_k, in_pairs)
+        pkv.kv_swap_blocks(t["v_cache"], host_v, in_pairs)
+
+    dev_buf = torch.empty(moved, dtype=torch.uint8, device="cuda")
+    host_buf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / args.steps
+
+    t_out, t_in = timed(swap_out), timed(swap_in)
+    if pkv.pkv_device_error() != 0:
+        raise RuntimeError("device error bits set during the swaps")
+    t_d2h = timed(lambda: host_buf.copy_(dev_buf, non_blocking=True))
+    t_h2d = timed(lambda: dev_buf.copy_(host_buf, non_blocking=True))
+    out_gbs, in_gbs = moved / t_out / 1e9, moved / t_in / 1e9
+    d2h_gbs, h2d_gbs = moved / t_d2h / 1e9, moved / t_h2d / 1e9
+    line = {
+        "metric": "paged KV block swap GB/s (device pool <-> pinned host pool, K+V)",
+        "value": round(2 * moved / (t_out + t_in) / 1e9, 2), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": w.name, "blocks_per_direction": n,
+                                        "block_bytes_per_tensor": block_bytes},
+        "swap_out_gbs": round(out_gbs, 2), "swap_in_gbs": round(in_gbs, 2),
+        "roofline": {"bound": "host link", "unit": "GB/s",
+                     "peak": {"d2h": round(d2h_gbs, 2), "h2d": round(h2d_gbs, 2)},
+                     "peak_source": "contiguous cudaMemcpyAsync of the same bytes, same run",
+                     "frac": {"out": round(out_gbs / d2h_gbs, 4), "in": round(in_gbs / h2d_gbs, 4)}},
+        "gpu_launches": 4 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.op == "swap":
+        run_swap(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -211,11 +211,49 @@ int paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache, con
                               pkv_dtype dtype, int partition_size, pkv_stream_t stream);
 
 /*
+ * kv_swap_blocks -- copy whole blocks from one pool to another (swap out / swap in).
+ *
+ * "PagedAttention" explainer, chapter 05 ("vLLM -- The Engine"): under memory pressure
+ * requests are recomputed or swapped out; "PagedAttention: how vLLM manages the KV cache",
+ * section "PagedAttention does not solve admission control": the scheduler must queue,
+ * preempt, recompute, swap or reject.  For each pair i,
+ *     dst_cache[dst_i] = src_cache[src_i]        (block_bytes bytes, bit-exact)
+ * with (src_i, dst_i) = (src_dst_pairs[2i], src_dst_pairs[2i+1]).  Unlike kv_copy_blocks
+ * the two pools are different tensors: either may be device memory or host memory the
+ * device can address (pinned host memory; on Grace-Blackwell the kernel reaches it over
+ * NVLink-C2C), so one launch gathers a preempted request's blocks out to a host pool, or
+ * back in.  Destination blocks must be distinct.  A pair naming an id outside its pool is
+ * skipped and sets PKV_DERR_PAIR.  Call once for the key pools and once for the value
+ * pools.
+ *
+ *   dst_cache      [dst_num_blocks] blocks of block_bytes bytes (written).
+ *   src_cache      [src_num_blocks] blocks of block_bytes bytes.
+ *   src_dst_pairs  int64 [num_pairs, 2], device-addressable memory.
+ * Returns PKV_OK, PKV_EINVAL or PKV_ECUDA.  num_pairs = 0 is a no-op.
+ */
+int kv_swap_blocks(void* dst_cache, const void* src_cache, const int64_t* src_dst_pairs,
+                   int num_pairs, size_t block_bytes, int dst_num_blocks, int src_num_blocks,
+                   pkv_stream_t stream);
+
+/*
  * Synchronise `stream`, then return and clear the device error bits (PKV_DERR_*) that
  * kernels of this library set on the current device since the last call.  Returns a
  * negative PKV_ECUDA if the synchronisation itself failed.
  */
 int pkv_device_error(pkv_stream_t stream);
+
+/*
+ * pkv_selftest_bounded_wait -- exercise the kernels' bounded-wait failure path.
+ *
+ * Launches one thread that waits on a fresh shared-memory mbarrier through the same
+ * bounded wait the decode pipeline uses, for at most `wait_us` microseconds (at most one
+ * second).  With arrive = 0 nothing ever completes the barrier, so the wait runs out,
+ * the kernel sets PKV_DERR_TIMEOUT and returns normally: the context stays usable and
+ * pkv_device_error() reports the bit.  With arrive != 0 the barrier completes at once
+ * and no bit is set.  Asynchronous on `stream`.  Returns PKV_OK, PKV_EINVAL or
+ * PKV_ECUDA.
+ */
+int pkv_selftest_bounded_wait(unsigned wait_us, int arrive, pkv_stream_t stream);
 
 /* Static description of a return code or device error bit. */
 const char* pkv_strerror(int code);

@@ -16,4 +16,5 @@ from .oracle import (  # noqa: F401
     paged_decode,
     paged_decode_partitioned,
     slot,
+    swap_blocks,
 )

@@ -62,6 +62,8 @@ def _load():
         lib.pkvo_kv_cache_write.restype = i32
         lib.pkvo_copy_blocks.argtypes = [P, P, i32, sz, i32]
         lib.pkvo_copy_blocks.restype = i32
+        lib.pkvo_swap_blocks.argtypes = [P, P, P, i32, sz, i32, i32]
+        lib.pkvo_swap_blocks.restype = i32
         lib.pkvo_num_blocks.argtypes = [i64, i32]
         lib.pkvo_num_blocks.restype = i64
         lib.pkvo_slot.argtypes = [P, i64, i32]
@@ -174,6 +176,24 @@ def copy_blocks(cache, src_dst_pairs) -> int:
     rc = _load().pkvo_copy_blocks(_ptr(cache), _ptr(pairs), int(pairs.shape[0]), block_bytes, NB)
     if rc < 0:
         raise ValueError(f"oracle copy_blocks rejected its inputs (code {rc})")
+    return int(rc)
+
+
+def swap_blocks(dst_cache, src_cache, src_dst_pairs) -> int:
+    """Copy whole blocks ``src_cache[src] -> dst_cache[dst]`` (two pools) in place.
+
+    Returns 0, or 1 when a pair with an out-of-range id was skipped.
+    """
+    if not dst_cache.flags.c_contiguous:
+        raise ValueError("dst_cache must be C-contiguous (written in place)")
+    src_cache = np.ascontiguousarray(src_cache)
+    if dst_cache[0].nbytes != src_cache[0].nbytes or dst_cache.dtype != src_cache.dtype:
+        raise ValueError("pools must have the same block size and element type")
+    pairs = _c(src_dst_pairs, np.int64).reshape(-1, 2)
+    rc = _load().pkvo_swap_blocks(_ptr(dst_cache), _ptr(src_cache), _ptr(pairs), int(pairs.shape[0]),
+                                  dst_cache[0].nbytes, dst_cache.shape[0], src_cache.shape[0])
+    if rc < 0:
+        raise ValueError(f"oracle swap_blocks rejected its inputs (code {rc})")
     return int(rc)
 
 

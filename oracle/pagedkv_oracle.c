@@ -345,6 +345,28 @@ int pkvo_copy_blocks(void* cache, const int64_t* src_dst_pairs, int num_pairs,
     return bad ? PKVO_EDATA : PKVO_OK;
 }
 
+/* ---- block copies between two pools (swap out / swap in) ---------------------------- */
+/*
+ * For each pair (src, dst): block dst of dst_cache becomes a byte copy of block src of
+ * src_cache.  "PagedAttention" (papermap), chapter 05 "vLLM -- The Engine": under memory
+ * pressure requests are swapped out or recomputed; "PagedAttention: how vLLM manages the
+ * KV cache", section "PagedAttention does not solve admission control": the scheduler
+ * must queue, preempt, recompute, swap or reject.  A pair naming an id outside its pool
+ * is skipped and PKVO_EDATA is returned.
+ */
+int pkvo_swap_blocks(void* dst_cache, const void* src_cache, const int64_t* src_dst_pairs,
+                     int num_pairs, size_t block_bytes, int dst_num_blocks, int src_num_blocks) {
+    if (num_pairs < 0 || dst_num_blocks < 0 || src_num_blocks < 0) return PKVO_EINVAL;
+    int bad = 0;
+    for (int i = 0; i < num_pairs; ++i) {
+        int64_t src = src_dst_pairs[2 * (size_t)i], dst = src_dst_pairs[2 * (size_t)i + 1];
+        if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) { bad = 1; continue; }
+        memcpy((char*)dst_cache + (size_t)dst * block_bytes,
+               (const char*)src_cache + (size_t)src * block_bytes, block_bytes);
+    }
+    return bad ? PKVO_EDATA : PKVO_OK;
+}
+
 int pkvo_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

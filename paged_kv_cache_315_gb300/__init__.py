@@ -6,7 +6,8 @@ A thin Python front end to ``libpagedkv.so`` (hand-written CUDA for sm_103a):
   tables, GQA heads batched per KV head, split-context partitions merged by
   log-sum-exp in the same launch;
 * ``kv_cache_write``     -- slot-mapped write of new tokens' keys and values;
-* ``kv_copy_blocks``     -- whole-block copies for copy-on-write.
+* ``kv_copy_blocks``     -- whole-block copies for copy-on-write;
+* ``kv_swap_blocks``     -- whole-block copies between pools (device / pinned host).
 
 The C ABI is declared in ``include/pagedkv.h``.  PyTorch is used only for device
 memory and streams.
@@ -24,12 +25,14 @@ from ._binding import (  # noqa: F401
     PagedKVError,
     kv_cache_write,
     kv_copy_blocks,
+    kv_swap_blocks,
     load,
     paged_attn_decode,
     paged_attn_decode_noalloc,
     paged_attn_decode_partition_tokens,
     paged_attn_decode_workspace_size,
     pkv_device_error,
+    pkv_selftest_bounded_wait,
     pkv_strerror,
     pkv_version,
     workspace_for,

@@ -64,6 +64,10 @@ def load() -> ctypes.CDLL:
         lib.kv_cache_write.restype = i32
         lib.kv_copy_blocks.argtypes = [P, P, i32, sz, i32, P]
         lib.kv_copy_blocks.restype = i32
+        lib.kv_swap_blocks.argtypes = [P, P, P, i32, sz, i32, i32, P]
+        lib.kv_swap_blocks.restype = i32
+        lib.pkv_selftest_bounded_wait.argtypes = [ctypes.c_uint, i32, P]
+        lib.pkv_selftest_bounded_wait.restype = i32
         lib.pkv_device_error.argtypes = [P]
         lib.pkv_device_error.restype = i32
         lib.pkv_strerror.argtypes = [i32]
@@ -115,6 +119,12 @@ def pkv_device_error(stream=None) -> int:
     if rc < 0:
         raise PagedKVError("pkv_device_error", rc)
     return rc
+
+
+def pkv_selftest_bounded_wait(wait_us: int, arrive: bool = False, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (see include/pagedkv.h)."""
+    _check("pkv_selftest_bounded_wait",
+           load().pkv_selftest_bounded_wait(int(wait_us), int(bool(arrive)), _stream(stream)))
 
 
 def paged_attn_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
@@ -247,3 +257,35 @@ def kv_copy_blocks(cache: torch.Tensor, src_dst_pairs: torch.Tensor, stream=None
     rc = load().kv_copy_blocks(_cuda("cache", cache), _cuda("src_dst_pairs", src_dst_pairs), P,
                                block_bytes, NB, _stream(stream))
     _check("kv_copy_blocks", rc)
+
+
+def _addressable(name: str, t: torch.Tensor) -> int:
+    """Pointer of a contiguous tensor the GPU can address: CUDA or pinned host memory."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+        raise TypeError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def kv_swap_blocks(dst_cache: torch.Tensor, src_cache: torch.Tensor, src_dst_pairs: torch.Tensor,
+                   stream=None) -> None:
+    """Copy whole blocks ``src_cache[src] -> dst_cache[dst]`` between two pools.
+
+    Either pool may live on the GPU or in pinned host memory (swap out / swap in).
+    """
+    if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or \
+            src_dst_pairs.shape[1] != 2:
+        raise TypeError("src_dst_pairs must be int64 [P, 2]")
+    if dst_cache[0].numel() * dst_cache.element_size() != \
+            src_cache[0].numel() * src_cache.element_size():
+        raise ValueError("the two pools must have the same block size")
+    P = src_dst_pairs.shape[0]
+    if P == 0:
+        return
+    block_bytes = dst_cache[0].numel() * dst_cache.element_size()
+    rc = load().kv_swap_blocks(_addressable("dst_cache", dst_cache),
+                               _addressable("src_cache", src_cache),
+                               _addressable("src_dst_pairs", src_dst_pairs), P, block_bytes,
+                               dst_cache.shape[0], src_cache.shape[0], _stream(stream))
+    _check("kv_swap_blocks", rc)

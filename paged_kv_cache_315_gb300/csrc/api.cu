@@ -5,6 +5,7 @@
 #include <climits>
 #include <mutex>
 
+#include "device_common.cuh"
 #include "internal.h"
 #include "pagedkv.h"
 
@@ -32,6 +33,19 @@ unsigned* error_word() {
 }
 
 bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// One thread waits on a fresh mbarrier, through the same bounded wait the pipelines use,
+// for at most `limit_ns`; the barrier completes only if `arrive` is set.  A wait that
+// runs out sets PKV_DERR_TIMEOUT and the kernel returns normally.
+__global__ void bounded_wait_selftest(unsigned long long limit_ns, int arrive, unsigned* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_addr(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  if (arrive) mbar_arrive_expect_tx(b, 0);
+  if (!mbar_wait_for(b, 0, limit_ns)) raise_error(err, PKV_DERR_TIMEOUT);
+}
 
 bool valid_dtype(pkv_dtype d) { return d == PKV_F32 || d == PKV_BF16 || d == PKV_F16; }
 
@@ -139,6 +153,29 @@ int kv_copy_blocks(void* cache, const int64_t* src_dst_pairs, int num_pairs, siz
   if (!err) return PKV_ECUDA;
   return launch_kv_copy_blocks(cache, src_dst_pairs, num_pairs, block_bytes, num_blocks, err,
                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kv_swap_blocks(void* dst_cache, const void* src_cache, const int64_t* src_dst_pairs,
+                   int num_pairs, size_t block_bytes, int dst_num_blocks, int src_num_blocks,
+                   pkv_stream_t stream) {
+  if (num_pairs < 0 || dst_num_blocks <= 0 || src_num_blocks <= 0 || block_bytes == 0)
+    return PKV_EINVAL;
+  if (num_pairs == 0) return PKV_OK;
+  if (!dst_cache || !src_cache || !src_dst_pairs || !aligned(src_dst_pairs, 8)) return PKV_EINVAL;
+  unsigned* err = error_word();
+  if (!err) return PKV_ECUDA;
+  return launch_kv_swap_blocks(dst_cache, src_cache, src_dst_pairs, num_pairs, block_bytes,
+                               dst_num_blocks, src_num_blocks, err,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pkv_selftest_bounded_wait(unsigned wait_us, int arrive, pkv_stream_t stream) {
+  if (wait_us > 1000000u) return PKV_EINVAL;
+  unsigned* err = error_word();
+  if (!err) return PKV_ECUDA;
+  bounded_wait_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<unsigned long long>(wait_us) * 1000ull, arrive, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 int pkv_device_error(pkv_stream_t stream) {

@@ -68,6 +68,30 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// dst block <- src block of another pool for every pair; either pool may be device
+// memory or host memory the device can address (pinned host memory, reached over
+// NVLink-C2C on Grace-Blackwell); blockIdx.y strides over pairs.
+template <typename V>
+__global__ void __launch_bounds__(kThreads)
+    kv_swap_kernel(V* __restrict__ dst, const V* __restrict__ src,
+                   const int64_t* __restrict__ pairs, int num_pairs, long long vec_per_block,
+                   long long dst_blocks, long long src_blocks, unsigned* err) {
+  for (int pi = blockIdx.y; pi < num_pairs; pi += gridDim.y) {
+    const long long s = __ldg(&pairs[2LL * pi]);
+    const long long d = __ldg(&pairs[2LL * pi + 1]);
+    if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) raise_error(err, PKV_DERR_PAIR);
+      continue;
+    }
+    const V* sp = src + s * vec_per_block;
+    V* dp = dst + d * vec_per_block;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+         i < vec_per_block; i += stride)
+      dp[i] = sp[i];
+  }
+}
+
 // Widest vector (16, 8, 4, 2 or 1 bytes) dividing `bytes` and every pointer's address.
 int vector_bytes(size_t bytes, std::initializer_list<const void*> ptrs) {
   for (int w : {16, 8, 4, 2}) {
@@ -106,7 +130,33 @@ int copy_with(void* cache, const int64_t* pairs, int num_pairs, size_t block_byt
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
+template <typename V>
+int swap_with(void* dst, const void* src, const int64_t* pairs, int num_pairs, size_t block_bytes,
+              int dst_blocks, int src_blocks, unsigned* err, cudaStream_t stream) {
+  const long long vpb = static_cast<long long>(block_bytes / sizeof(V));
+  const long long per_pair = std::max(1LL, (vpb + 4LL * kThreads - 1) / (4LL * kThreads));
+  const int gy = std::min(num_pairs, 65535);
+  const int gx = static_cast<int>(std::min(per_pair, 1024LL));
+  kv_swap_kernel<V><<<dim3(gx, gy), kThreads, 0, stream>>>(
+      static_cast<V*>(dst), static_cast<const V*>(src), pairs, num_pairs, vpb, dst_blocks,
+      src_blocks, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
 }  // namespace
+
+int launch_kv_swap_blocks(void* dst, const void* src, const int64_t* pairs, int num_pairs,
+                          size_t block_bytes, int dst_blocks, int src_blocks, unsigned* err,
+                          cudaStream_t stream) {
+  if (num_pairs == 0) return PKV_OK;
+  switch (vector_bytes(block_bytes, {dst, src})) {
+    case 16: return swap_with<uint4>(dst, src, pairs, num_pairs, block_bytes, dst_blocks, src_blocks, err, stream);
+    case 8: return swap_with<uint2>(dst, src, pairs, num_pairs, block_bytes, dst_blocks, src_blocks, err, stream);
+    case 4: return swap_with<uint32_t>(dst, src, pairs, num_pairs, block_bytes, dst_blocks, src_blocks, err, stream);
+    case 2: return swap_with<uint16_t>(dst, src, pairs, num_pairs, block_bytes, dst_blocks, src_blocks, err, stream);
+    default: return swap_with<uint8_t>(dst, src, pairs, num_pairs, block_bytes, dst_blocks, src_blocks, err, stream);
+  }
+}
 
 int launch_kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
                           const int64_t* slot_mapping, int num_tokens, size_t row_bytes,

@@ -57,6 +57,10 @@ int launch_kv_cache_write(const void* k, const void* v, void* k_cache, void* v_c
 int launch_kv_copy_blocks(void* cache, const int64_t* pairs, int num_pairs, size_t block_bytes,
                           int num_blocks, unsigned* err, cudaStream_t stream);
 
+int launch_kv_swap_blocks(void* dst, const void* src, const int64_t* pairs, int num_pairs,
+                          size_t block_bytes, int dst_blocks, int src_blocks, unsigned* err,
+                          cudaStream_t stream);
+
 size_t dtype_size(pkv_dtype dtype);
 
 }  // namespace pkv

@@ -372,3 +372,75 @@ def test_config5_long_context_split(pkv):
     assert pkv.pkv_device_error() == 0
     seqs = _sample(w, 3, 5)
     assert_close(host_out(out)[seqs], oracle_decode(w, seqs=seqs), "bf16", "config 5")
+
+
+# ------------------------------------------------------------------------------------------
+# failure detection: a wait that runs out is reported, and the context stays usable
+# ------------------------------------------------------------------------------------------
+
+def test_bounded_wait_runs_out_and_reports(pkv):
+    import time
+
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    pkv.pkv_selftest_bounded_wait(20000, arrive=False)       # nothing ever arrives
+    assert pkv.pkv_device_error() == pkv.PKV_DERR_TIMEOUT
+    waited = time.perf_counter() - t0
+    assert 0.015 < waited < 1.0
+    pkv.pkv_selftest_bounded_wait(20000, arrive=True)        # completes at once
+    assert pkv.pkv_device_error() == 0
+    # the context is still usable: a decode right after gives the oracle's answer
+    w = synth.make_workload("after", seed=77, dtype="bf16", context_lens=[40, 700],
+                            num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16)
+    t = synth.to_torch(w, "cuda")
+    assert_close(host_out(gpu_decode(pkv, w, t)), oracle_decode(w), "bf16", "after timeout")
+
+
+# ------------------------------------------------------------------------------------------
+# swap out / swap in between the device pool and a pinned host pool
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,bs,Hkv,D", [("bf16", 16, 8, 128), ("f32", 32, 2, 64),
+                                            ("f16", 16, 1, 24)])
+def test_swap_out_to_host_and_back_in_bit_exact(pkv, dtype, bs, Hkv, D):
+    w = synth.make_workload("sw", seed=21, dtype=dtype, context_lens=[bs * 30, bs * 7 + 3],
+                            num_q_heads=Hkv, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                            pool_slack=1.0)
+    t = synth.to_torch(w, "cuda")
+    nb = -(-int(w.context_lens[1]) // bs)
+    blocks = w.block_tables[1, :nb].astype(np.int64)
+    host_shape = (12,) + tuple(t["k_cache"].shape[1:])
+    hk = torch.zeros(host_shape, dtype=t["k_cache"].dtype).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    out_pairs = np.stack([blocks, np.arange(nb) + 3], axis=1)
+    tp = torch.from_numpy(out_pairs).cuda()
+    pkv.kv_swap_blocks(hk, t["k_cache"], tp)                   # device -> host
+    pkv.kv_swap_blocks(hv, t["v_cache"], tp)
+    assert pkv.pkv_device_error() == 0
+    hk_ref = np.zeros((12,) + w.k_cache.shape[1:], w.k_cache.dtype)
+    hv_ref = np.zeros_like(hk_ref)
+    oracle.swap_blocks(hk_ref, w.k_cache, out_pairs)
+    oracle.swap_blocks(hv_ref, w.v_cache, out_pairs)
+    assert np.array_equal(synth.tensor_to_storage(hk), hk_ref)
+    assert np.array_equal(synth.tensor_to_storage(hv), hv_ref)
+    # swap back in to fresh device blocks, pairs given in pinned host memory
+    used = set(w.block_tables[w.block_tables >= 0].tolist())
+    free = np.array([b for b in range(w.num_blocks) if b not in used][:nb], np.int64)
+    in_pairs = np.stack([np.arange(nb) + 3, free], axis=1)
+    tin = torch.from_numpy(in_pairs).pin_memory()
+    pkv.kv_swap_blocks(t["k_cache"], hk, tin)                   # host -> device
+    pkv.kv_swap_blocks(t["v_cache"], hv, tin)
+    assert pkv.pkv_device_error() == 0
+    k_ref, v_ref = w.k_cache.copy(), w.v_cache.copy()
+    oracle.swap_blocks(k_ref, hk_ref, in_pairs)
+    oracle.swap_blocks(v_ref, hv_ref, in_pairs)
+    assert np.array_equal(synth.tensor_to_storage(t["k_cache"]), k_ref)
+    assert np.array_equal(synth.tensor_to_storage(t["v_cache"]), v_ref)
+
+
+def test_swap_flags_ids_outside_either_pool(pkv):
+    dev = torch.arange(4 * 16 * 64, dtype=torch.float32, device="cuda").view(4, 16, 1, 64)
+    host = torch.zeros(2, 16, 1, 64).pin_memory()
+    pkv.kv_swap_blocks(host, dev, torch.tensor([[3, 1], [0, 2], [9, 0]], device="cuda"))
+    assert pkv.pkv_device_error() == pkv.PKV_DERR_PAIR
+    assert torch.equal(host[1], dev[3].cpu()) and host[0].eq(0).all()

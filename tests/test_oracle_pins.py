@@ -443,3 +443,44 @@ def test_copy_on_write_leaves_other_sharers_unchanged(oracle_mod):
     ref = oracle_mod.paged_decode(w.q[1:2], kc2, vc2, np.array([[0, 1]], np.int32),
                                   np.array([21], np.int32), w.scale, "bf16")
     np.testing.assert_allclose(after[1], ref[0], rtol=1e-13, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------------------
+# block copies between pools (swap out / swap in)
+# ----------------------------------------------------------------------------------------
+
+def test_swap_out_and_back_in_restores_the_sequence(oracle_mod):
+    """Swapping a sequence's blocks to a host pool and back into other device blocks
+    (with its table renamed) leaves its attention output bit-identical; the pools' other
+    blocks are untouched.  Catches: swapped src/dst, copying from the wrong pool."""
+    w = _wl(dtype="bf16", lens=(40, 70), Hq=4, Hkv=2, D=64, bs=16, pool_slack=1.5)
+    before = _run(oracle_mod, w)
+    nb = -(-70 // 16)
+    blocks = w.block_tables[1, :nb].astype(np.int64)
+    host_k = np.zeros((8,) + w.k_cache.shape[1:], np.uint16)
+    host_v = np.zeros_like(host_k)
+    out_pairs = np.stack([blocks, np.arange(nb) + 2], axis=1)       # device -> host slots 2..
+    assert oracle_mod.swap_blocks(host_k, w.k_cache, out_pairs) == 0
+    assert oracle_mod.swap_blocks(host_v, w.v_cache, out_pairs) == 0
+    np.testing.assert_array_equal(host_k[2:2 + nb], w.k_cache[blocks])
+    assert (host_k[:2] == 0).all() and (host_k[2 + nb:] == 0).all()
+    used = set(w.block_tables[w.block_tables >= 0].tolist())
+    free = np.array([b for b in range(w.num_blocks) if b not in used][:nb], np.int64)
+    k2, v2 = w.k_cache.copy(), w.v_cache.copy()
+    k2[blocks] = 0                                                  # the old blocks are reused
+    v2[blocks] = 0
+    in_pairs = np.stack([np.arange(nb) + 2, free], axis=1)          # host -> new device blocks
+    assert oracle_mod.swap_blocks(k2, host_k, in_pairs) == 0
+    assert oracle_mod.swap_blocks(v2, host_v, in_pairs) == 0
+    bt = w.block_tables.copy()
+    bt[1, :nb] = free
+    after = oracle_mod.paged_decode(w.q, k2, v2, bt, w.context_lens, w.scale, "bf16")
+    np.testing.assert_array_equal(after, before)
+
+
+def test_swap_flags_ids_outside_either_pool(oracle_mod):
+    a = np.arange(4 * 8, dtype=np.float32).reshape(4, 2, 1, 4)
+    b = np.zeros((2, 2, 1, 4), np.float32)
+    assert oracle_mod.swap_blocks(b, a, np.array([[3, 1], [0, 2], [4, 0]])) == 1
+    np.testing.assert_array_equal(b[1], a[3])
+    assert (b[0] == 0).all()
