@@ -9,11 +9,15 @@ from .oracle import (  # noqa: F401
     DTYPE_CODES,
     build,
     copy_blocks,
+    e4m3_from_double,
+    e4m3_to_double,
     kv_cache_write,
+    kv_cache_write_fp8,
     locate,
     max_threads,
     num_blocks,
     paged_decode,
+    paged_decode_fp8kv,
     paged_decode_partitioned,
     slot,
     swap_blocks,

@@ -64,6 +64,16 @@ def _load():
         lib.pkvo_copy_blocks.restype = i32
         lib.pkvo_swap_blocks.argtypes = [P, P, P, i32, sz, i32, i32]
         lib.pkvo_swap_blocks.restype = i32
+        lib.pkvo_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.pkvo_e4m3_to_double.restype = dbl
+        lib.pkvo_e4m3_from_double.argtypes = [dbl]
+        lib.pkvo_e4m3_from_double.restype = ctypes.c_uint8
+        lib.pkvo_paged_decode_fp8kv.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, i32,
+                                                i32, i32, dbl, dbl, dbl, i32]
+        lib.pkvo_paged_decode_fp8kv.restype = i32
+        lib.pkvo_kv_cache_write_fp8.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32,
+                                                ctypes.c_float, ctypes.c_float]
+        lib.pkvo_kv_cache_write_fp8.restype = i32
         lib.pkvo_num_blocks.argtypes = [i64, i32]
         lib.pkvo_num_blocks.restype = i64
         lib.pkvo_slot.argtypes = [P, i64, i32]
@@ -194,6 +204,62 @@ def swap_blocks(dst_cache, src_cache, src_dst_pairs) -> int:
                                   dst_cache[0].nbytes, dst_cache.shape[0], src_cache.shape[0])
     if rc < 0:
         raise ValueError(f"oracle swap_blocks rejected its inputs (code {rc})")
+    return int(rc)
+
+
+def e4m3_to_double(codes) -> np.ndarray:
+    """Values of E4M3 codes (uint8), exactly, as float64."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.vectorize(lambda x: lib.pkvo_e4m3_to_double(int(x)), otypes=[np.float64])(c)
+
+
+def e4m3_from_double(x) -> np.ndarray:
+    """Nearest E4M3 codes (ties to even, saturating at +-448) of float64 values."""
+    lib = _load()
+    a = np.asarray(x, dtype=np.float64)
+    return np.vectorize(lambda v: lib.pkvo_e4m3_from_double(float(v)), otypes=[np.uint8])(a)
+
+
+def paged_decode_fp8kv(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+                       q_dtype, num_threads: int = 0) -> np.ndarray:
+    """fp64 decode over E4M3 caches (uint8 codes); q in ``q_dtype`` storage."""
+    q = _check_storage("q", q, q_dtype)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or k_cache.shape != v_cache.shape or bt.shape[0] != B or cl.shape != (B,):
+        raise ValueError("shape mismatch")
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    rc = _load().pkvo_paged_decode_fp8kv(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         DTYPE_CODES[q_dtype], _ptr(bt), _ptr(cl), B, Hq, Hkv, D,
+                                         bs, bt.shape[1], NB, float(scale), float(k_scale),
+                                         float(v_scale), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle paged_decode_fp8kv rejected its inputs (code {rc})")
+    return out
+
+
+def kv_cache_write_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale, dtype) -> int:
+    """Quantise token rows k[i], v[i] ([N, Hkv, D] in ``dtype`` storage) into the E4M3
+    caches (uint8 [NB, bs, Hkv, D], written in place) at row slot_mapping[i]."""
+    if not (k_cache.flags.c_contiguous and v_cache.flags.c_contiguous):
+        raise ValueError("caches must be C-contiguous (written in place)")
+    k = _check_storage("k", k, dtype)
+    v = _check_storage("v", v, dtype)
+    sm = _c(slot_mapping, np.int64)
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    row = int(np.prod(k_cache.shape[2:]))
+    if k[0].size != row:
+        raise ValueError("token rows must match the cache rows")
+    rc = _load().pkvo_kv_cache_write_fp8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(sm),
+                                         int(sm.shape[0]), row, DTYPE_CODES[dtype], NB, bs,
+                                         float(k_scale), float(v_scale))
+    if rc < 0:
+        raise ValueError(f"oracle kv_cache_write_fp8 rejected its inputs (code {rc})")
     return int(rc)
 
 

@@ -367,6 +367,132 @@ int pkvo_swap_blocks(void* dst_cache, const void* src_cache, const int64_t* src_
     return bad ? PKVO_EDATA : PKVO_OK;
 }
 
+/* ---- fp8 (E4M3) KV blocks --------------------------------------------------------- */
+/*
+ * "PagedAttention: how vLLM manages the KV cache", section "Keep the tensor formula beside
+ * the allocator model": lower-precision cache formats reduce the bytes per element.  The
+ * cache then holds 8-bit E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 fraction
+ * bits; no infinities; the all-ones pattern 0x7F / 0xFF is NaN; largest finite 448), and
+ * a per-tensor scale: the stored element stands for code_value * scale.
+ */
+
+double pkvo_e4m3_to_double(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);  /* subnormal: (m / 8) * 2^(1 - 7) */
+    else
+        v = ldexp((double)(m + 8), e - 10);  /* (1 + m/8) * 2^(e - 7) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to x (ties to the even code), magnitudes above 448 saturating to
+ * +-448; NaN maps to 0x7F.  Found by search over the 127 non-negative finite codes, which
+ * are ordered by value. */
+uint8_t pkvo_e4m3_from_double(double x) {
+    if (x != x) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double vc = pkvo_e4m3_to_double((uint8_t)c), vb = pkvo_e4m3_to_double((uint8_t)best);
+        double dc = fabs(vc - a), db = fabs(vb - a);
+        if (dc < db || (dc == db && (c & 1) == 0 && (best & 1) == 1)) best = c;
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Decode with fp8 caches: K_p = e4m3(k_code) * k_scale, V_p = e4m3(v_code) * v_scale; q in
+ * `dtype` (0 f32, 1 bf16, 2 f16).  Otherwise the same definition as pkvo_paged_decode. */
+int pkvo_paged_decode_fp8kv(double* out, const void* q, const uint8_t* k_cache,
+                            const uint8_t* v_cache, int dtype, const int32_t* block_tables,
+                            const int32_t* context_lens, int num_seqs, int num_q_heads,
+                            int num_kv_heads, int head_dim, int block_size,
+                            int max_blocks_per_seq, int num_blocks, double scale, double k_scale,
+                            double v_scale, int num_threads) {
+    if (!check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      max_blocks_per_seq, num_blocks, dtype))
+        return PKVO_EINVAL;
+    if (!check_tables(block_tables, context_lens, num_seqs, block_size, max_blocks_per_seq,
+                      num_blocks))
+        return PKVO_EINVAL;
+    int group = num_q_heads / num_kv_heads;
+    int64_t units = (int64_t)num_seqs * num_q_heads;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        int s = (int)(u / num_q_heads);
+        int h = (int)(u % num_q_heads);
+        int g = h / group;
+        double* o = out + (size_t)u * head_dim;
+        int64_t L = context_lens[s];
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        if (L == 0) continue;
+        const int32_t* bt_row = block_tables + (size_t)s * max_blocks_per_seq;
+        size_t qbase = ((size_t)s * num_q_heads + h) * (size_t)head_dim;
+        double* w = (double*)malloc((size_t)L * sizeof(double));
+        if (!w) { failed = 1; continue; }
+        for (int64_t p = 0; p < L; ++p) {
+            int32_t phys, off;
+            pkvo_locate(bt_row, p, block_size, &phys, &off);
+            double dot = 0.0;
+            for (int d = 0; d < head_dim; ++d)
+                dot += elem(q, qbase + d, dtype) *
+                       (pkvo_e4m3_to_double(k_cache[cache_index(phys, off, g, d, block_size,
+                                                                num_kv_heads, head_dim)]) *
+                        k_scale);
+            w[p] = scale * dot;
+        }
+        double m = -INFINITY;
+        for (int64_t p = 0; p < L; ++p) if (w[p] > m) m = w[p];
+        double z = 0.0;
+        for (int64_t p = 0; p < L; ++p) { w[p] = exp(w[p] - m); z += w[p]; }
+        for (int64_t p = 0; p < L; ++p) {
+            int32_t phys, off;
+            pkvo_locate(bt_row, p, block_size, &phys, &off);
+            for (int d = 0; d < head_dim; ++d)
+                o[d] += w[p] * (pkvo_e4m3_to_double(v_cache[cache_index(
+                                    phys, off, g, d, block_size, num_kv_heads, head_dim)]) *
+                                v_scale);
+        }
+        for (int d = 0; d < head_dim; ++d) o[d] /= z;
+        free(w);
+    }
+    return failed ? PKVO_ENOMEM : PKVO_OK;
+}
+
+/* Slot write into fp8 caches: each element x of token i's key row becomes the code of
+ * (x / k_scale) -- the division done in fp32, the precision the GPU writes with -- at row
+ * slot_mapping[i] (same for values with v_scale).  Slot rules as pkvo_kv_cache_write. */
+int pkvo_kv_cache_write_fp8(const void* k, const void* v, uint8_t* k_cache, uint8_t* v_cache,
+                            const int64_t* slot_mapping, int num_tokens, int row_elems,
+                            int dtype, int num_blocks, int block_size, float k_scale,
+                            float v_scale) {
+    if (num_tokens < 0 || num_blocks < 0 || block_size <= 0 || row_elems <= 0) return PKVO_EINVAL;
+    int64_t rows = (int64_t)num_blocks * block_size;
+    int bad = 0;
+    for (int i = 0; i < num_tokens; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        if (slot >= rows) { bad = 1; continue; }
+        for (int e = 0; e < row_elems; ++e) {
+            size_t src = (size_t)i * row_elems + e, dst = (size_t)slot * row_elems + e;
+            float xk = (float)elem(k, src, dtype) / k_scale;
+            float xv = (float)elem(v, src, dtype) / v_scale;
+            k_cache[dst] = pkvo_e4m3_from_double((double)xk);
+            v_cache[dst] = pkvo_e4m3_from_double((double)xv);
+        }
+    }
+    return bad ? PKVO_EDATA : PKVO_OK;
+}
+
 int pkvo_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

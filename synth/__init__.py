@@ -6,7 +6,8 @@ It holds none of the attention arithmetic.  It only
 
   * draws random tensors (``numpy`` counter-seeded generators, one independent
     stream per tensor and per chunk, so results do not depend on thread count),
-  * rounds fp32 draws to bf16 / fp16 storage,
+  * rounds fp32 draws to bf16 / fp16 storage, and re-encodes pools as E4M3 codes for
+    fp8 caches (torch's float8 conversion),
   * hands out physical blocks with a trivial allocator: the pool's ids are shuffled
     once and each sequence takes the next ``ceil(L / block_size)`` of them in order,
   * records, from that allocation, which cache slots hold live tokens (for
@@ -401,6 +402,23 @@ def storage_to_torch(a: np.ndarray, dtype: str, device):
     if dtype != "f32":
         t = t.view(torch.int16).view({"bf16": torch.bfloat16, "f16": torch.float16}[dtype])
     return t.to(device)
+
+
+def e4m3_codes(values: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 codes (uint8) of values / scale, by torch's float8_e4m3fn conversion (nearest,
+    ties to even) after clamping to the format's +-448."""
+    import torch
+
+    x = torch.from_numpy(np.ascontiguousarray(values, dtype=np.float32)) / np.float32(scale)
+    x = x.clamp(-448.0, 448.0)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def fp8_kv(w: Workload, k_scale: float, v_scale: float):
+    """The workload's K and V pools re-encoded as E4M3 codes with per-tensor scales."""
+    k = storage_to_f64(w.k_cache, w.dtype).astype(np.float32)
+    v = storage_to_f64(w.v_cache, w.dtype).astype(np.float32)
+    return e4m3_codes(k, k_scale), e4m3_codes(v, v_scale)
 
 
 def to_torch(w: Workload, device):

@@ -484,3 +484,79 @@ def test_swap_flags_ids_outside_either_pool(oracle_mod):
     assert oracle_mod.swap_blocks(b, a, np.array([[3, 1], [0, 2], [4, 0]])) == 1
     np.testing.assert_array_equal(b[1], a[3])
     assert (b[0] == 0).all()
+
+
+# ----------------------------------------------------------------------------------------
+# fp8 (E4M3) KV blocks
+# ----------------------------------------------------------------------------------------
+
+def test_e4m3_values_match_torch(oracle_mod):
+    """All 256 codes decode to torch's float8_e4m3fn values (NaN where torch has NaN)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(oracle_mod.e4m3_to_double(codes), ref)
+
+
+def test_e4m3_rounding_matches_torch(oracle_mod):
+    """Encoding rounds to nearest, ties to even, and saturates at 448 like torch's
+    conversion of clamped values.  Catches: truncation, ties away from zero, overflow."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = oracle_mod.e4m3_to_double(codes)
+    np.testing.assert_array_equal(oracle_mod.e4m3_from_double(vals), codes)   # round trip
+    finite = np.sort(np.unique(vals))
+    mids = (finite[1:] + finite[:-1]) / 2                                       # exact ties
+    rng = np.random.default_rng(8)
+    x = np.concatenate([mids, rng.standard_normal(4000) * 40, rng.standard_normal(500) * 1e-2,
+                        [500.0, -1e4, 447.9, 449.0]]).astype(np.float32)
+    ref = torch.from_numpy(np.clip(x, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle_mod.e4m3_from_double(x.astype(np.float64)), ref)
+
+
+def test_fp8_decode_equals_decode_of_dequantised_cache(oracle_mod):
+    """With power-of-two scales the dequantised cache is exact in fp32, so the fp8 decode
+    must equal the plain decode of that cache, and SDPA on it.  Catches: a scale applied
+    to the wrong tensor, or twice."""
+    w = _wl(dtype="bf16", lens=(1, 16, 37, 200), Hq=8, Hkv=2, D=64, bs=16, shuffle=False)
+    ks, vs = 2.0 ** -4, 2.0 ** -3
+    k8, v8 = synth.fp8_kv(w, ks, vs)
+    out = oracle_mod.paged_decode_fp8kv(w.q, k8, v8, w.block_tables, w.context_lens, w.scale,
+                                        ks, vs, "bf16")
+    kf = (oracle_mod.e4m3_to_double(k8) * ks).astype(np.float32)
+    vf = (oracle_mod.e4m3_to_double(v8) * vs).astype(np.float32)
+    qf = synth.storage_to_f64(w.q, "bf16").astype(np.float32)
+    ref = oracle_mod.paged_decode(qf, kf, vf, w.block_tables, w.context_lens, w.scale, "f32")
+    np.testing.assert_array_equal(out, ref)
+    NB, bs = kf.shape[:2]
+    for s in range(w.num_seqs):
+        start, L = int(w.block_tables[s, 0]) * bs, int(w.context_lens[s])
+        K = torch.from_numpy(kf.reshape(NB * bs, 2, 64)[start:start + L].astype(np.float64))
+        V = torch.from_numpy(vf.reshape(NB * bs, 2, 64)[start:start + L].astype(np.float64))
+        qt = torch.from_numpy(qf[s].astype(np.float64))[:, None, :]
+        sd = torch.nn.functional.scaled_dot_product_attention(
+            qt, K.permute(1, 0, 2).repeat_interleave(4, 0), V.permute(1, 0, 2).repeat_interleave(4, 0),
+            scale=w.scale)
+        np.testing.assert_allclose(out[s], sd[:, 0].numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_fp8_slot_write_quantises_like_torch(oracle_mod):
+    """A new token's rows become the codes torch gives x / scale (fp32 division), in the
+    slot's row.  Catches: multiplying by the scale, rounding before the division."""
+    NB, bs, Hkv, D = 6, 16, 2, 32
+    rng = np.random.default_rng(3)
+    k_new = synth.to_storage(rng.standard_normal((5, Hkv, D)) * 3, "bf16")
+    v_new = synth.to_storage(rng.standard_normal((5, Hkv, D)) * 3, "bf16")
+    kc = np.zeros((NB, bs, Hkv, D), np.uint8)
+    vc = np.zeros_like(kc)
+    slots = np.array([0, 17, -1, 95, 40], np.int64)
+    ks, vs = 0.0371, 0.05
+    assert oracle_mod.kv_cache_write_fp8(k_new, v_new, kc, vc, slots, ks, vs, "bf16") == 0
+    rows_k = kc.reshape(NB * bs, Hkv, D)
+    rows_v = vc.reshape(NB * bs, Hkv, D)
+    kx = synth.storage_to_f64(k_new, "bf16").astype(np.float32)
+    vx = synth.storage_to_f64(v_new, "bf16").astype(np.float32)
+    for i, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        np.testing.assert_array_equal(rows_k[sl], synth.e4m3_codes(kx[i], ks))
+        np.testing.assert_array_equal(rows_v[sl], synth.e4m3_codes(vx[i], vs))
+    assert (rows_k[[1, 2, 3]] == 0).all()
