@@ -42,10 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # beside it (profiles/ holds the captures).
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each
-    "13b-mha-b64-bf16@2048": {"bytes": 1408906000 + 4161792, "decode_cu_sha": "13d0b5ae3ca7754a"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 964765696 + 8224512, "decode_cu_sha": "13d0b5ae3ca7754a"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328558848 + 4712704, "decode_cu_sha": "13d0b5ae3ca7754a"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4327292416 + 36300032, "decode_cu_sha": "13d0b5ae3ca7754a"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408788480 + 3472640, "decode_cu_sha": "d951b0d02173d71c"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 964699648 + 7546624, "decode_cu_sha": "d951b0d02173d71c"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328653056 + 6000384, "decode_cu_sha": "d951b0d02173d71c"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4326800896 + 36461568, "decode_cu_sha": "d951b0d02173d71c"},
+    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704839424 + 3758336, "decode_cu_sha": "d951b0d02173d71c"},
+    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483400192 + 6973952, "decode_cu_sha": "d951b0d02173d71c"},
+    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164931840 + 4155648, "decode_cu_sha": "d951b0d02173d71c"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2162245376 + 35482112, "decode_cu_sha": "d951b0d02173d71c"},
 }
 
 
@@ -63,6 +67,8 @@ def parse_args(argv=None):
                    help="CPU time budget of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--kv-dtype", choices=["same", "fp8"], default="same",
+                   help="cache element type: the batch's own (default) or fp8 E4M3 codes")
     p.add_argument("--op", choices=["decode", "swap"], default="decode",
                    help="decode (default): the decode step; swap: block swaps device <-> host")
     p.add_argument("--swap-blocks", type=int, default=4096,
@@ -92,10 +98,19 @@ def bench_workload(cfg: int) -> synth.Workload:
     return w
 
 
-def algorithmic_bytes(w: synth.Workload) -> dict:
+def fp8_scales(cfg: int) -> tuple[float, float]:
+    """Per-tensor scales for E4M3 caches: N(0,1) data (x8 key outliers in batch 5)."""
+    return (0.125, 0.0625) if cfg == 5 else (0.0625, 0.0625)
+
+
+def kv_bytes(w: synth.Workload, fp8: bool) -> int:
+    return w.kv_bytes() // w.elem_bytes if fp8 else w.kv_bytes()
+
+
+def algorithmic_bytes(w: synth.Workload, fp8: bool = False) -> dict:
     """Bytes the decode launch must move at minimum, and its parts."""
     e = w.elem_bytes
-    kv = w.kv_bytes()
+    kv = kv_bytes(w, fp8)
     q = w.q.size * e
     out = q
     nblocks = int(sum((int(L) + w.block_size - 1) // w.block_size for L in w.context_lens))
@@ -199,8 +214,8 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-def traffic_for(w_name: str, part: int) -> float | None:
-    entry = MEASURED_TRAFFIC.get(f"{w_name}@{part}")
+def traffic_for(w_name: str, part: int, fp8: bool = False) -> float | None:
+    entry = MEASURED_TRAFFIC.get(f"{w_name}@{part}" + ("+fp8" if fp8 else ""))
     if not entry:
         return None
     import hashlib
@@ -252,14 +267,25 @@ def run_ours(args) -> None:
     w = bench_workload(cfg)
     part = w.partition_size if args.partition < 0 else args.partition
     t = synth.to_torch(w, dev)
+    fp8 = args.kv_dtype == "fp8"
+    if fp8:
+        ks, vs = fp8_scales(cfg)
+        k8, v8 = synth.fp8_kv(w, ks, vs)
+        t["k_cache"] = torch.from_numpy(k8).to(dev)
+        t["v_cache"] = torch.from_numpy(v8).to(dev)
+        del k8, v8
+    step_kv_bytes = kv_bytes(w, fp8)
     if cfg == 4:
         # state: copy-on-write copies, then every suffix token
         pkv.kv_copy_blocks(t["k_cache"], t["copy_pairs"])
         pkv.kv_copy_blocks(t["v_cache"], t["copy_pairs"])
-        pkv.kv_cache_write(synth.storage_to_torch(w.info["setup_k"], "bf16", dev),
-                           synth.storage_to_torch(w.info["setup_v"], "bf16", dev),
-                           t["k_cache"], t["v_cache"],
-                           torch.from_numpy(w.info["setup_slots"]).to(dev))
+        sk = synth.storage_to_torch(w.info["setup_k"], "bf16", dev)
+        sv = synth.storage_to_torch(w.info["setup_v"], "bf16", dev)
+        ss = torch.from_numpy(w.info["setup_slots"]).to(dev)
+        if args.kv_dtype == "fp8":
+            pkv.kv_cache_write_fp8(sk, sv, t["k_cache"], t["v_cache"], ss, *fp8_scales(cfg))
+        else:
+            pkv.kv_cache_write(sk, sv, t["k_cache"], t["v_cache"], ss)
     out = torch.empty_like(t["q"])
     B = w.num_seqs
     part = pkv.paged_attn_decode_partition_tokens(B, w.num_q_heads, w.num_kv_heads, w.block_size,
@@ -272,12 +298,21 @@ def run_ours(args) -> None:
         if has_pairs:
             pkv.kv_copy_blocks(t["k_cache"], inp["copy_pairs"])
             pkv.kv_copy_blocks(t["v_cache"], inp["copy_pairs"])
-        pkv.kv_cache_write(inp["k_new"], inp["v_new"], t["k_cache"], t["v_cache"],
-                           inp["slot_mapping"])
+        if fp8:
+            pkv.kv_cache_write_fp8(inp["k_new"], inp["v_new"], t["k_cache"], t["v_cache"],
+                                   inp["slot_mapping"], ks, vs)
+        else:
+            pkv.kv_cache_write(inp["k_new"], inp["v_new"], t["k_cache"], t["v_cache"],
+                               inp["slot_mapping"])
         if ev is not None:
             ev[0].record()
-        pkv.paged_attn_decode(out, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
-                              inp["context_lens"], w.scale, partition_size=part, workspace=ws)
+        if fp8:
+            pkv.paged_attn_decode_fp8(out, inp["q"], t["k_cache"], t["v_cache"],
+                                      inp["block_tables"], inp["context_lens"], w.scale, ks, vs,
+                                      partition_size=part, workspace=ws)
+        else:
+            pkv.paged_attn_decode(out, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
+                                  inp["context_lens"], w.scale, partition_size=part, workspace=ws)
         if ev is not None:
             ev[1].record()
 
@@ -341,7 +376,7 @@ def run_ours(args) -> None:
         barrier()
         e2e_s = time.perf_counter() - s0
         (e2e_s,) = max_over_ranks([e2e_s], world)
-        e2e = {"value": round(replica_gbs(w.kv_bytes(), args.steps, world, e2e_s), 2), "unit": "GB/s",
+        e2e = {"value": round(replica_gbs(step_kv_bytes, args.steps, world, e2e_s), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e2e_s * 1e3 / args.steps, 4),
                "path": "pinned host inputs -> cudaMemcpyAsync -> C-ABI calls -> output to "
@@ -349,16 +384,16 @@ def run_ours(args) -> None:
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds)
+        cpu = cpu_baseline(w, args.cpu_seconds, fp8_scales(cfg) if fp8 else None)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
     peak, peak_kind = hbm_peak()
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, fp8)
     ms = elapsed_ms / args.steps
-    value = replica_gbs(w.kv_bytes(), args.steps, world, elapsed_ms / 1e3)
+    value = replica_gbs(step_kv_bytes, args.steps, world, elapsed_ms / 1e3)
     achieved = ab["total"] / (decode_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
@@ -371,7 +406,7 @@ def run_ours(args) -> None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.dtype,
+        "dtype": w.dtype if not fp8 else f"{w.dtype} (E4M3 KV cache)",
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
         "config": describe(w, cfg, part),
         "hbm_frac": round(value / peak, 4),
@@ -379,11 +414,13 @@ def run_ours(args) -> None:
         "query_heads_per_s": round(B * w.num_q_heads * world / (ms / 1e3), 1),
         "decode_ms": round(decode_ms, 5),
         "partition_tokens": part,
-        "roofline": {"kernel": "paged_attn_decode (decode_tc_kernel)", "bound": "hbm",
+        "kv_dtype": "e4m3" if fp8 else w.dtype,
+        "roofline": {"kernel": "paged_attn_decode_fp8 (decode_fp8_kernel)" if fp8
+                     else "paged_attn_decode (decode_tc_kernel)", "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": ab,
-                     "traffic": traffic_for(w.name, part)},
+                     "traffic": traffic_for(w.name, part, fp8)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -398,9 +435,13 @@ def run_ours(args) -> None:
 # the oracle on the host cores (CPU baseline and reference arm)
 # ------------------------------------------------------------------------------------------
 
-def _oracle_seq(w, s):
+def _oracle_seq(w, s, fp8=None):
     import oracle
 
+    if fp8 is not None:
+        k8, v8, ks, vs = fp8
+        return oracle.paged_decode_fp8kv(w.q[s:s + 1], k8, v8, w.block_tables[s:s + 1],
+                                         w.context_lens[s:s + 1], w.scale, ks, vs, w.dtype)
     return oracle.paged_decode(w.q[s:s + 1], w.k_cache, w.v_cache, w.block_tables[s:s + 1],
                                w.context_lens[s:s + 1], w.scale, w.dtype)
 
@@ -409,17 +450,20 @@ def seq_kv_bytes(w, s) -> int:
     return int(w.context_lens[s]) * 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
 
 
-def cpu_baseline(w, seconds: float) -> dict:
+def cpu_baseline(w, seconds: float, fp8_scale_pair=None) -> dict:
     """The fp64 oracle, as it stands, over sequences of the batch until ``seconds`` pass."""
     import oracle
 
     oracle.build()
+    fp8 = None
+    if fp8_scale_pair is not None:
+        fp8 = (*synth.fp8_kv(w, *fp8_scale_pair), *fp8_scale_pair)
     done_bytes, done_seqs = 0, 0
     s0 = time.perf_counter()
     while True:
         s = done_seqs % w.num_seqs
-        _oracle_seq(w, s)
-        done_bytes += seq_kv_bytes(w, s)
+        _oracle_seq(w, s, fp8)
+        done_bytes += seq_kv_bytes(w, s) // (w.elem_bytes if fp8 else 1)
         done_seqs += 1
         el = time.perf_counter() - s0
         if el >= seconds or done_seqs >= 4 * w.num_seqs:

@@ -160,6 +160,45 @@ int kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
                    int block_size, int num_blocks, pkv_dtype dtype, pkv_stream_t stream);
 
 /*
+ * paged_attn_decode_fp8 -- paged_attn_decode over caches of 8-bit E4M3 codes.
+ *
+ * "PagedAttention: how vLLM manages the KV cache", section "Keep the tensor formula
+ * beside the allocator model": lower-precision cache formats reduce the bytes per element
+ * (paging itself does not).  k_cache and v_cache hold E4M3 codes (uint8, 1 sign, 4
+ * exponent bits with bias 7, 3 fraction bits, largest finite 448), laid out
+ * [num_blocks, block_size, num_kv_heads, head_dim] like the 16-bit caches; element e
+ * stands for value(e) * k_scale (keys) or value(e) * v_scale (values), per-tensor scales.
+ * The result is paged_attn_decode's on those values:
+ *     out[s][h] = sum_p softmax_p( scale * <q[s][h], K_p> ) * V_p.
+ * q and out are `dtype` (PKV_BF16 or PKV_F16).  Codes convert exactly to fp16, so the
+ * products run on the tensor cores in fp16 with fp32 accumulation.  head_dim must be 128
+ * and block_size 16, 32 or 64.  Other arguments, the workspace and the return codes are
+ * those of paged_attn_decode (the same workspace size).
+ */
+int paged_attn_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int max_blocks_per_seq, int num_blocks, float scale, float k_scale,
+                          float v_scale, pkv_dtype dtype, int partition_size, void* workspace,
+                          size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * kv_cache_write_fp8 -- kv_cache_write into E4M3 caches.
+ *
+ * Element x of token i's key row becomes the E4M3 code nearest to x / k_scale (the
+ * division in IEEE fp32; ties to the even code; magnitudes beyond 448 saturate to +-448;
+ * NaN stays NaN), stored at row slot_mapping[i] of k_cache; likewise for values with
+ * v_scale.  k and v are [num_tokens, num_kv_heads, head_dim] in `dtype` (any of the three
+ * types); num_kv_heads * head_dim must be a multiple of 8.  Slot rules and return codes
+ * are those of kv_cache_write.  The copies are deterministic: equal inputs give equal
+ * codes.
+ */
+int kv_cache_write_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                       const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                       int head_dim, int block_size, int num_blocks, pkv_dtype dtype,
+                       float k_scale, float v_scale, pkv_stream_t stream);
+
+/*
  * kv_copy_blocks -- copy whole physical blocks of one cache tensor, for copy-on-write.
  *
  * "PagedAttention: how vLLM manages the KV cache", section "Copy-on-write makes shared

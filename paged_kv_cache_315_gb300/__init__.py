@@ -24,10 +24,12 @@ from ._binding import (  # noqa: F401
     PKV_F32,
     PagedKVError,
     kv_cache_write,
+    kv_cache_write_fp8,
     kv_copy_blocks,
     kv_swap_blocks,
     load,
     paged_attn_decode,
+    paged_attn_decode_fp8,
     paged_attn_decode_noalloc,
     paged_attn_decode_partition_tokens,
     paged_attn_decode_workspace_size,

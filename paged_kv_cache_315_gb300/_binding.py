@@ -64,6 +64,12 @@ def load() -> ctypes.CDLL:
         lib.kv_cache_write.restype = i32
         lib.kv_copy_blocks.argtypes = [P, P, i32, sz, i32, P]
         lib.kv_copy_blocks.restype = i32
+        lib.paged_attn_decode_fp8.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                              i32, f32, f32, f32, i32, i32, P, sz, P]
+        lib.paged_attn_decode_fp8.restype = i32
+        lib.kv_cache_write_fp8.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, f32,
+                                           P]
+        lib.kv_cache_write_fp8.restype = i32
         lib.kv_swap_blocks.argtypes = [P, P, P, i32, sz, i32, i32, P]
         lib.kv_swap_blocks.restype = i32
         lib.pkv_selftest_bounded_wait.argtypes = [ctypes.c_uint, i32, P]
@@ -289,3 +295,60 @@ def kv_swap_blocks(dst_cache: torch.Tensor, src_cache: torch.Tensor, src_dst_pai
                                _addressable("src_dst_pairs", src_dst_pairs), P, block_bytes,
                                dst_cache.shape[0], src_cache.shape[0], _stream(stream))
     _check("kv_swap_blocks", rc)
+
+
+def _fp8_cache(name: str, t: torch.Tensor) -> int:
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{name} must hold E4M3 codes as torch.uint8")
+    return _cuda(name, t)
+
+
+def paged_attn_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                          v_cache: torch.Tensor, block_tables: torch.Tensor,
+                          context_lens: torch.Tensor, scale: float, k_scale: float,
+                          v_scale: float, partition_size: int = 0,
+                          workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode over E4M3 caches (uint8 codes [NB, bs, Hkv, D]); q / out bf16 or fp16."""
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if q.dtype != out.dtype:
+        raise TypeError("q and out must share one element type")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    MB = block_tables.shape[1]
+    need = paged_attn_decode_workspace_size(B, Hq, Hkv, D, bs, MB, partition_size)
+    if workspace is None:
+        workspace = workspace_for(q.device, need)
+    ws_ptr = _cuda("workspace", workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().paged_attn_decode_fp8(
+        _cuda("out", out), _cuda("q", q), _fp8_cache("k_cache", k_cache),
+        _fp8_cache("v_cache", v_cache), _cuda("block_tables", block_tables),
+        _cuda("context_lens", context_lens), B, Hq, Hkv, D, bs, MB, NB, float(scale),
+        float(k_scale), float(v_scale), _dtype(q), int(partition_size), ws_ptr, ws_bytes,
+        _stream(stream))
+    _check("paged_attn_decode_fp8", rc)
+    return out
+
+
+def kv_cache_write_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                       v_scale: float, stream=None) -> None:
+    """Quantise token rows k[i] / v[i] [N, Hkv, D] into E4M3 cache slot slot_mapping[i]."""
+    NB, bs, Hkv, D = k_cache.shape
+    N = k.shape[0]
+    if tuple(k.shape) != (N, Hkv, D) or tuple(v.shape) != (N, Hkv, D):
+        raise ValueError("k and v must be [N, Hkv, D] matching the cache")
+    if k.dtype != v.dtype:
+        raise TypeError("k and v must share one element type")
+    if slot_mapping.dtype != torch.int64 or tuple(slot_mapping.shape) != (N,):
+        raise TypeError("slot_mapping must be int64 [N]")
+    if N == 0:
+        return
+    rc = load().kv_cache_write_fp8(_cuda("k", k), _cuda("v", v), _fp8_cache("k_cache", k_cache),
+                                   _fp8_cache("v_cache", v_cache),
+                                   _cuda("slot_mapping", slot_mapping), N, Hkv, D, bs, NB,
+                                   _dtype(k), float(k_scale), float(v_scale), _stream(stream))
+    _check("kv_cache_write_fp8", rc)

@@ -103,6 +103,57 @@ int paged_attn_decode(void* out, const void* q, const void* k_cache, const void*
   return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int paged_attn_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int max_blocks_per_seq, int num_blocks, float scale, float k_scale,
+                          float v_scale, pkv_dtype dtype, int partition_size, void* workspace,
+                          size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      block_size <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || !valid_dtype(dtype))
+    return PKV_EINVAL;
+  if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f)) return PKV_EINVAL;
+  if (static_cast<long long>(num_blocks) * block_size >= INT_MAX) return PKV_EINVAL;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size >= INT_MAX) return PKV_EINVAL;
+  const int ptok = resolve_partition_tokens(partition_size, block_size, num_seqs, num_q_heads,
+                                            num_kv_heads, max_blocks_per_seq);
+  if (ptok < 0) return PKV_EINVAL;
+  if (!decode_fp8_supported(dtype, head_dim, block_size)) return PKV_EUNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_EINVAL;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 4) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return PKV_EINVAL;
+  if (workspace && !aligned(workspace, 16)) return PKV_EINVAL;
+  unsigned* err = error_word();
+  if (!err) return PKV_ECUDA;
+  DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.partition_tokens = ptok;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err = err;
+  a.kv_fp8 = true;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                         int head_dim, int block_size, int max_blocks_per_seq,
                                         int partition_size) {
@@ -142,6 +193,27 @@ int kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
   const long long rows = static_cast<long long>(num_blocks) * block_size;
   return launch_kv_cache_write(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, rows,
                                err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kv_cache_write_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                       const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                       int head_dim, int block_size, int num_blocks, pkv_dtype dtype,
+                       float k_scale, float v_scale, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      num_blocks <= 0 || !valid_dtype(dtype))
+    return PKV_EINVAL;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f)) return PKV_EINVAL;
+  const long long row_elems = static_cast<long long>(num_kv_heads) * head_dim;
+  if (row_elems % 8 != 0 || row_elems > INT_MAX) return PKV_EINVAL;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_EINVAL;
+  if (!aligned(slot_mapping, 8) || !aligned(k_cache, 8) || !aligned(v_cache, 8)) return PKV_EINVAL;
+  unsigned* err = error_word();
+  if (!err) return PKV_ECUDA;
+  return launch_kv_cache_write_fp8(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                   static_cast<int>(row_elems), dtype,
+                                   static_cast<long long>(num_blocks) * block_size, k_scale,
+                                   v_scale, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kv_copy_blocks(void* cache, const int64_t* src_dst_pairs, int num_pairs, size_t block_bytes,

@@ -3,6 +3,8 @@
 // Both are pure byte movement, bound by HBM bandwidth: each thread moves 16-byte vectors
 // (narrower only when a size or pointer is not 16-byte aligned), grid-stride, with the
 // grid sized to a multiple of the SM count.
+#include <cuda_fp8.h>
+
 #include <algorithm>
 
 #include "device_common.cuh"
@@ -92,6 +94,46 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// k_cache row `slot` <- E4M3 codes of k row i / k_scale (and v with v_scale); one thread
+// per 8 elements.  The division is IEEE fp32; the conversion rounds to nearest even and
+// saturates at +-448.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    kv_write_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                        uint8_t* __restrict__ kc, uint8_t* __restrict__ vc,
+                        const int64_t* __restrict__ slots, long long num_tokens, int row_elems,
+                        long long num_rows, float k_scale, float v_scale, unsigned* err) {
+  const int groups = row_elems / 8;
+  const long long total = num_tokens * groups;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const long long t = i / groups;
+    const int e0 = static_cast<int>(i - t * groups) * 8;
+    const long long slot = __ldg(&slots[t]);
+    if (slot < 0) continue;
+    if (slot >= num_rows) {
+      if (e0 == 0) raise_error(err, PKV_DERR_SLOT);
+      continue;
+    }
+    uint8_t ck[8], cv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float xk = __fdiv_rn(to_f32(k[t * row_elems + e0 + e]), k_scale);
+      const float xv = __fdiv_rn(to_f32(v[t * row_elems + e0 + e]), v_scale);
+      ck[e] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(xk, __NV_SATFINITE, __NV_E4M3));
+      cv[e] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(xv, __NV_SATFINITE, __NV_E4M3));
+    }
+    uint2 pk, pv;
+    pk.x = ck[0] | (ck[1] << 8) | (ck[2] << 16) | (static_cast<uint32_t>(ck[3]) << 24);
+    pk.y = ck[4] | (ck[5] << 8) | (ck[6] << 16) | (static_cast<uint32_t>(ck[7]) << 24);
+    pv.x = cv[0] | (cv[1] << 8) | (cv[2] << 16) | (static_cast<uint32_t>(cv[3]) << 24);
+    pv.y = cv[4] | (cv[5] << 8) | (cv[6] << 16) | (static_cast<uint32_t>(cv[7]) << 24);
+    *reinterpret_cast<uint2*>(kc + slot * row_elems + e0) = pk;
+    *reinterpret_cast<uint2*>(vc + slot * row_elems + e0) = pv;
+  }
+}
+
 // Widest vector (16, 8, 4, 2 or 1 bytes) dividing `bytes` and every pointer's address.
 int vector_bytes(size_t bytes, std::initializer_list<const void*> ptrs) {
   for (int w : {16, 8, 4, 2}) {
@@ -169,6 +211,35 @@ int launch_kv_cache_write(const void* k, const void* v, void* k_cache, void* v_c
     case 2: return write_with<uint16_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, num_rows, err, stream);
     default: return write_with<uint8_t>(k, v, k_cache, v_cache, slot_mapping, num_tokens, row_bytes, num_rows, err, stream);
   }
+}
+
+int launch_kv_cache_write_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                              const int64_t* slot_mapping, int num_tokens, int row_elems,
+                              pkv_dtype src_dtype, long long num_rows, float k_scale,
+                              float v_scale, unsigned* err, cudaStream_t stream) {
+  if (num_tokens == 0) return PKV_OK;
+  const long long total = static_cast<long long>(num_tokens) * (row_elems / 8);
+  const int grid = static_cast<int>(
+      std::max(1LL, std::min((total + kThreads - 1) / kThreads, 8LL * sm_count())));
+  uint8_t* kc = static_cast<uint8_t*>(k_cache);
+  uint8_t* vc = static_cast<uint8_t*>(v_cache);
+  switch (src_dtype) {
+    case PKV_F32:
+      kv_write_fp8_kernel<float><<<grid, kThreads, 0, stream>>>(
+          static_cast<const float*>(k), static_cast<const float*>(v), kc, vc, slot_mapping,
+          num_tokens, row_elems, num_rows, k_scale, v_scale, err);
+      break;
+    case PKV_BF16:
+      kv_write_fp8_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), kc, vc,
+          slot_mapping, num_tokens, row_elems, num_rows, k_scale, v_scale, err);
+      break;
+    default:
+      kv_write_fp8_kernel<__half><<<grid, kThreads, 0, stream>>>(
+          static_cast<const __half*>(k), static_cast<const __half*>(v), kc, vc, slot_mapping,
+          num_tokens, row_elems, num_rows, k_scale, v_scale, err);
+  }
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 int launch_kv_copy_blocks(void* cache, const int64_t* pairs, int num_pairs, size_t block_bytes,

@@ -43,6 +43,7 @@ constexpr int kTcHeads = 16;    // query heads per CTA on the tensor-core path
 constexpr int kSimtHeads = 8;   // ... on the CUDA-core path
 constexpr int kMaxStageSet = 4; // stages per warp, at most
 constexpr int kMaxParts = 1024; // partitions per sequence, at most
+constexpr float kRescaleSlack = 8.f;  // see online_softmax
 constexpr long long kMinUnits = 2048;  // work units the default partition size aims for
 
 struct Params {
@@ -60,7 +61,9 @@ struct Params {
   int tile_bytes;   // bytes of one K (or V) tile
   int tile_stride;  // tile_bytes rounded up to 1024: V tile offset inside a stage
   int stage_bytes, box_bytes, box_cols, boxes, ring_bytes;
+  int pair;         // physical blocks per staged tile (2 pairs 16-token blocks for fp8)
   float scale_log2;
+  float out_scale;  // multiplies every output (the V scale of fp8 caches, else 1)
 };
 
 struct Work {
@@ -151,17 +154,24 @@ __device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, c
                                                const CUtensorMap* kmap, const CUtensorMap* vmap,
                                                int x0, int spec_id);
 
+// Load staged tile v: physical blocks v*pair .. v*pair + pair - 1 of the partition (those
+// that exist), stacked row-wise so that two 16-row boxes form the layout of one 32-row box.
 __device__ __forceinline__ void issue_tile(const Params& P, const Smem& sm, const CUtensorMap* kmap,
-                                           const CUtensorMap* vmap, int j, int x0) {
-  const int st = j % P.stages;
+                                           const CUtensorMap* vmap, int v, int x0, int nblk) {
+  const int st = v % P.stages;
   const uint32_t bar = smem_addr(&sm.bars[st]);
   const uint32_t kdst = smem_addr(sm.ring + st * P.stage_bytes);
   const uint32_t vdst = kdst + P.tile_stride;
-  const int y = sm.ycoord[j];
-  mbar_arrive_expect_tx(bar, 2u * P.tile_bytes);
-  for (int b = 0; b < P.boxes; ++b) {
-    tma_load_2d(kdst + b * P.box_bytes, kmap, bar, x0 + b * P.box_cols, y);
-    tma_load_2d(vdst + b * P.box_bytes, vmap, bar, x0 + b * P.box_cols, y);
+  const int j0 = v * P.pair;
+  const int cnt = min(P.pair, nblk - j0);
+  mbar_arrive_expect_tx(bar, 2u * cnt * P.tile_bytes);
+  for (int i = 0; i < cnt; ++i) {
+    const int y = sm.ycoord[j0 + i];
+    for (int b = 0; b < P.boxes; ++b) {
+      const uint32_t off = b * P.pair * P.box_bytes + i * P.box_bytes;
+      tma_load_2d(kdst + off, kmap, bar, x0 + b * P.box_cols, y);
+      tma_load_2d(vdst + off, vmap, bar, x0 + b * P.box_cols, y);
+    }
   }
 }
 
@@ -188,15 +198,16 @@ __device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, c
   if (tid == 0) {
     tma_prefetch_desc(kmap);
     tma_prefetch_desc(vmap);
-    const int first = min(P.stages, w.nblk);
-    for (int j = 0; j < first; ++j) issue_tile(P, sm, kmap, vmap, j, x0);
+    const int nv = (w.nblk + P.pair - 1) / P.pair;
+    const int first = min(P.stages, nv);
+    for (int v = 0; v < first; ++v) issue_tile(P, sm, kmap, vmap, v, x0, w.nblk);
   }
 }
 
 // After a timed-out wait on block j: wait (bounded) for this warp's loads still in flight.
 __device__ __forceinline__ void drain_after_timeout(const Params& P, const Work& w, const Smem& sm,
                                                     int j) {
-  const int end = min(w.nblk, j + P.stages);
+  const int end = min((w.nblk + P.pair - 1) / P.pair, j + P.stages);
   for (int jj = j; jj < end; jj += kWarps)
     mbar_wait_bounded(smem_addr(&sm.bars[jj % P.stages]), (jj / P.stages) & 1);
 }
@@ -226,7 +237,7 @@ __device__ void finish(const Params& P, const Work& w, int D, int HC, const floa
     }
     const size_t row = static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r;
     if (!split) {
-      out[row * D + d] = from_f32<T>(num / den);
+      out[row * D + d] = from_f32<T>(num / den * P.out_scale);
     } else {
       const size_t idx = row * P.max_parts + w.p;
       P.ws_o[idx * D + d] = num;
@@ -271,7 +282,7 @@ __device__ void finish(const Params& P, const Work& w, int D, int HC, const floa
     const size_t base = row * P.max_parts;
     float acc = 0.f;
     for (int p = 0; p < w.np; ++p) acc += wts[r * w.np + p] * __ldcg(&P.ws_o[(base + p) * D + d]);
-    out[row * D + d] = from_f32<T>(acc);
+    out[row * D + d] = from_f32<T>(acc * P.out_scale);
   }
 }
 
@@ -284,6 +295,69 @@ __device__ void finish(const Params& P, const Work& w, int D, int HC, const floa
 template <int BS>
 __device__ __forceinline__ uint32_t swz(int r, int d) {
   return static_cast<uint32_t>((d >> 6) * (BS * 128) + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4));
+}
+
+// One block's online-softmax step on the S fragments of an m16n8 tile row pair: scale into
+// log2 units, mask tokens past `valid`, update the running max m and sum l (rows lane/4
+// and lane/4 + 8), rescale the output accumulators, and return P = 2^(S - m) rounded to
+// the operand type as A fragments for P.V.  The row sums use the rounded weights.
+template <typename T, int BS, int ND>
+__device__ __forceinline__ void online_softmax(float (&sc)[BS / 8][4], float (&o)[ND][4],
+                                               float (&m)[2], float (&l)[2],
+                                               uint32_t (&pa)[BS / 16][4], int valid,
+                                               float scale_log2, int lane) {
+  constexpr int NT = BS / 8;
+  // scale into log2 units, mask tokens past the context, row maxima over the quad
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int tok = nt * 8 + (lane & 3) * 2 + (c & 1);
+      const float v = sc[nt][c] * scale_log2;
+      sc[nt][c] = tok < valid ? v : -INFINITY;
+    }
+    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
+    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  // The reference max m moves only when a row's new scores exceed it by more than
+  // kRescaleSlack (log2 units): the weights 2^(S - m) then stay below 2^kRescaleSlack,
+  // and the accumulators are rescaled only on those (rare) blocks.  o and l always share
+  // one m, so the final o / l is unchanged.
+  const bool up0 = mx0 > m[0] + kRescaleSlack, up1 = mx1 > m[1] + kRescaleSlack;
+  const float mn0 = up0 ? mx0 : m[0], mn1 = up1 ? mx1 : m[1];
+  // P = 2^(S - m) rounded to the operand type; the row sums use the rounded weights
+  float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint32_t lo = Mma<T>::pack(exp2f(sc[nt][0] - mn0), exp2f(sc[nt][1] - mn0));
+    const uint32_t hi = Mma<T>::pack(exp2f(sc[nt][2] - mn1), exp2f(sc[nt][3] - mn1));
+    const float2 flo = Mma<T>::unpack(lo), fhi = Mma<T>::unpack(hi);
+    rs0 += flo.x + flo.y;
+    rs1 += fhi.x + fhi.y;
+    pa[nt >> 1][(nt & 1) * 2 + 0] = lo;
+    pa[nt >> 1][(nt & 1) * 2 + 1] = hi;
+  }
+  if (__any_sync(0xffffffffu, up0 || up1)) {
+    const float a0 = exp2f(m[0] - mn0), a1 = exp2f(m[1] - mn1);  // 1 for rows that kept m
+    l[0] *= a0;
+    l[1] *= a1;
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd) {
+      o[nd][0] *= a0;
+      o[nd][1] *= a0;
+      o[nd][2] *= a1;
+      o[nd][3] *= a1;
+    }
+  }
+  m[0] = mn0;
+  m[1] = mn1;
+  l[0] += rs0;
+  l[1] += rs1;
 }
 
 template <typename T, int D, int BS>
@@ -308,49 +382,8 @@ __device__ __forceinline__ void tc_block(uint32_t kb, uint32_t vb, const uint32_
       Mma<T>::run(sc[nt], qa[kk + 1], b2, b3);
     }
   }
-  // scale into log2 units, mask tokens past the context, row maxima over the quad
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int tok = nt * 8 + (lane & 3) * 2 + (c & 1);
-      const float v = sc[nt][c] * scale_log2;
-      sc[nt][c] = tok < valid ? v : -INFINITY;
-    }
-    mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
-    mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
-  }
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-  const float a0 = exp2f(m[0] - mn0), a1 = exp2f(m[1] - mn1);
-  m[0] = mn0;
-  m[1] = mn1;
-  // P = 2^(S - m) rounded to the operand type; the row sums use the rounded weights
   uint32_t pa[BS / 16][4];
-  float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const uint32_t lo = Mma<T>::pack(exp2f(sc[nt][0] - mn0), exp2f(sc[nt][1] - mn0));
-    const uint32_t hi = Mma<T>::pack(exp2f(sc[nt][2] - mn1), exp2f(sc[nt][3] - mn1));
-    const float2 flo = Mma<T>::unpack(lo), fhi = Mma<T>::unpack(hi);
-    rs0 += flo.x + flo.y;
-    rs1 += fhi.x + fhi.y;
-    pa[nt >> 1][(nt & 1) * 2 + 0] = lo;
-    pa[nt >> 1][(nt & 1) * 2 + 1] = hi;
-  }
-  l[0] = l[0] * a0 + rs0;
-  l[1] = l[1] * a1 + rs1;
-#pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) {
-    o[nd][0] *= a0;
-    o[nd][1] *= a0;
-    o[nd][2] *= a1;
-    o[nd][3] *= a1;
-  }
+  online_softmax<T, BS, D / 8>(sc, o, m, l, pa, valid, scale_log2, lane);
   // O += P . V : B = V rows via transposing ldmatrix.
 #pragma unroll
   for (int kt = 0; kt < BS / 16; ++kt) {
@@ -432,7 +465,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     tc_block<T, D, BS>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
     __syncwarp();
-    if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0);
+    if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0, w.nblk);
   }
 
   __syncthreads();  // all stages consumed: the ring becomes the merge buffer
@@ -444,6 +477,165 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd) {
       const int col = nd * 8 + (lane & 3) * 2;
+      if (r0 < w.hc)
+        *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0) * D + col]) = make_float2(o[nd][0], o[nd][1]);
+      if (r0 + 8 < w.hc)
+        *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0 + 8) * D + col]) =
+            make_float2(o[nd][2], o[nd][3]);
+    }
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
+    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
+    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+    if ((lane & 3) == 0) {
+      if (r0 < w.hc) {
+        ml_s[(warp * kTcHeads + r0) * 2] = m[0];
+        ml_s[(warp * kTcHeads + r0) * 2 + 1] = l[0];
+      }
+      if (r0 + 8 < w.hc) {
+        ml_s[(warp * kTcHeads + r0 + 8) * 2] = m[1];
+        ml_s[(warp * kTcHeads + r0 + 8) * 2 + 1] = l[1];
+      }
+    }
+  }
+  __syncthreads();
+  finish<T>(P, w, D, kTcHeads, O_s, ml_s, wts, sm.flags);
+}
+
+// ------------------------------------------------------------------------------------------
+// fp8 (E4M3) caches: tensor cores in fp16
+// ------------------------------------------------------------------------------------------
+//
+// K and V tiles hold E4M3 codes: rows of head_dim = 128 bytes, one TMA box with the
+// 128-byte swizzle.  Every E4M3 value is exactly an fp16 value, so Q is converted to fp16
+// and both products run as fp16 mma with fp32 accumulation; the K scale is folded into
+// the score scale and the V scale multiplies the output.  head_dim is visited in an order
+// that is the same for Q and K (a dot product does not depend on the order of its terms):
+// lane c = lane % 4 of a quad owns elements [32c, 32c + 32), so a lane's operand bytes of
+// one row are 32 contiguous bytes.  For P.V the lanes own V's columns the same way; an 8x8
+// block of V (8 tokens x 8 columns) is read row-wise and transposed in registers with
+// movmatrix, and column j of output n-tile nd is head_dim element 32(j/2) + 2nd + j%2.
+
+// Byte offset of 16-byte chunk `chunk` of row r in a tile of 128-byte rows stored with the
+// TMA 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz_chunk(int r, int chunk) {
+  return static_cast<uint32_t>(r * 128 + ((chunk ^ (r & 7)) << 4));
+}
+
+template <int BS>
+__device__ __forceinline__ void fp8_block(uint32_t kb, uint32_t vb, const uint32_t (&qa)[8][4],
+                                          float (&o)[16][4], float (&m)[2], float (&l)[2],
+                                          int valid, float scale_log2, int lane) {
+  constexpr int NT = BS / 8;
+  const int c = lane & 3, r8 = lane >> 2;
+  float sc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    const int r = nt * 8 + r8;
+    const uint4 w0 = lds128(kb + swz_chunk(r, 2 * c));
+    const uint4 w1 = lds128(kb + swz_chunk(r, 2 * c + 1));
+    const uint32_t wk[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t b0, b1;
+      e4m3x4_to_f16x2x2(wk[kk], b0, b1);
+      Mma<__half>::run(sc[nt], qa[kk], b0, b1);
+    }
+  }
+  uint32_t pa[BS / 16][4];
+  online_softmax<__half, BS, 16>(sc, o, m, l, pa, valid, scale_log2, lane);
+#pragma unroll
+  for (int kt = 0; kt < BS / 16; ++kt) {
+    const int ra = kt * 16 + r8, rb = ra + 8;
+    const uint4 a0 = lds128(vb + swz_chunk(ra, 2 * c)), a1 = lds128(vb + swz_chunk(ra, 2 * c + 1));
+    const uint4 b0 = lds128(vb + swz_chunk(rb, 2 * c)), b1 = lds128(vb + swz_chunk(rb, 2 * c + 1));
+    const uint32_t va[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t vc[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t a_even, a_odd, c_even, c_odd;  // columns of n-tiles 2i and 2i+1
+      e4m3x4_to_f16x2x2(va[i], a_even, a_odd);
+      e4m3x4_to_f16x2x2(vc[i], c_even, c_odd);
+      Mma<__half>::run(o[2 * i], pa[kt], movmatrix_trans(a_even), movmatrix_trans(c_even));
+      Mma<__half>::run(o[2 * i + 1], pa[kt], movmatrix_trans(a_odd), movmatrix_trans(c_odd));
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t to_f16x2(uint32_t w, __half) { return w; }
+__device__ __forceinline__ uint32_t to_f16x2(uint32_t w, __nv_bfloat16) {
+  const float2 f = Mma<__nv_bfloat16>::unpack(w);
+  return Mma<__half>::pack(f.x, f.y);
+}
+
+template <typename T, int BS, int PAIR>
+__global__ void __launch_bounds__(kThreads)
+    decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const Params P) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  Work w;
+  int spec_id;
+  if (!decode_work<T>(P, D, w, spec_id)) return;
+  const Smem sm = carve(smem_raw, P);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int x0 = w.g * D;  // bytes of one KV head's row segment
+  pipeline_start(P, w, sm, &kmap, &vmap, x0, spec_id);
+
+  // Q fragments in fp16, head_dim visited as described above
+  uint32_t qa[8][4];
+  {
+    const T* qs = static_cast<const T*>(P.q) + (static_cast<size_t>(w.s) * P.num_q_heads + w.h0) * D;
+    const int r0 = lane >> 2, c = lane & 3;
+    auto ld = [&](int r, int d) {
+      return r < w.hc ? to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qs + r * D + d)), T()) : 0u;
+    };
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int d0 = 32 * c + 4 * kk;
+      qa[kk][0] = ld(r0, d0);
+      qa[kk][1] = ld(r0 + 8, d0);
+      qa[kk][2] = ld(r0, d0 + 2);
+      qa[kk][3] = ld(r0 + 8, d0 + 2);
+    }
+  }
+  float o[16][4];
+#pragma unroll
+  for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+  constexpr int TR = BS * PAIR;  // token rows of a staged tile
+  const int nv = (w.nblk + PAIR - 1) / PAIR;
+  for (int v = warp; v < nv; v += kWarps) {
+    const int st = v % P.stages;
+    if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (v / P.stages) & 1)) {
+      if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
+      drain_after_timeout(P, w, sm, v);
+      break;
+    }
+    uint8_t* ktile = sm.ring + st * P.stage_bytes;
+    uint8_t* vtile = ktile + P.tile_stride;
+    const int valid = min(TR, w.tok_valid - v * TR);
+    if (valid < TR) {
+      zero_tail_rows<64, TR>(vtile, valid, lane);  // 128-byte rows, one box
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+    fp8_block<TR>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
+    __syncwarp();
+    if (lane == 0 && v + P.stages < nv) issue_tile(P, sm, &kmap, &vmap, v + P.stages, x0, w.nblk);
+  }
+
+  __syncthreads();
+  float* O_s = reinterpret_cast<float*>(sm.ring);
+  float* ml_s = O_s + kWarps * kTcHeads * D;
+  float* wts = ml_s + kWarps * kTcHeads * 2;
+  {
+    const int r0 = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+      const int col = 32 * c + 2 * nd;
       if (r0 < w.hc)
         *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0) * D + col]) = make_float2(o[nd][0], o[nd][1]);
       if (r0 + 8 < w.hc)
@@ -541,7 +733,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     __syncwarp();
-    if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0);
+    if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0, w.nblk);
   }
 
   __syncthreads();
@@ -587,15 +779,17 @@ EncodeTiledFn encode_fn() {
 }
 
 // The cache seen as a 2-D tensor: x = num_kv_heads * head_dim elements, y = cache rows.
-bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dt, int Hkv, int D,
+bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dt, bool fp8, int Hkv, int D,
                     long long rows, int box_cols, int box_rows, bool swizzle) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const CUtensorMapDataType t = dt == PKV_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+  const CUtensorMapDataType t = fp8              ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                : dt == PKV_F32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                 : dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const size_t esize = fp8 ? 1 : dtype_size(dt);
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(Hkv) * D, static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hkv) * D * dtype_size(dt)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(Hkv) * D * esize};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, t, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -632,6 +826,14 @@ KernelFn simt_kernel_for(int D) {
   }
 }
 
+template <typename T>
+KernelFn fp8_kernel_for(int BS) {
+  if (BS == 16) return decode_fp8_kernel<T, 16, 2>;  // two 16-token blocks per staged tile
+  if (BS == 32) return decode_fp8_kernel<T, 32, 1>;
+  if (BS == 64) return decode_fp8_kernel<T, 64, 1>;
+  return nullptr;
+}
+
 KernelFn kernel_for(pkv_dtype dt, int D, int BS, bool tc) {
   if (tc) {
     if (dt == PKV_BF16) return tc_kernel_for<__nv_bfloat16>(D, BS);
@@ -649,10 +851,11 @@ struct Geometry {
   int stages, tile_bytes, tile_stride, stage_bytes, ring_bytes, smem_bytes;
 };
 
-Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, int max_parts) {
+Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, int max_parts,
+                  bool fp8 = false, int pair = 1) {
   Geometry g{};
-  g.tile_bytes = BS * D * static_cast<int>(dtype_size(dt));
-  g.tile_stride = static_cast<int>(align_up(g.tile_bytes, 1024));
+  g.tile_bytes = BS * D * (fp8 ? 1 : static_cast<int>(dtype_size(dt)));
+  g.tile_stride = static_cast<int>(align_up(static_cast<size_t>(pair) * g.tile_bytes, 1024));
   g.stage_bytes = 2 * g.tile_stride;
   const int per_warp = std::max(1, std::min(kMaxStageSet, 16384 / g.stage_bytes));
   g.stages = kWarps * per_warp;
@@ -722,9 +925,16 @@ bool decode_supported(pkv_dtype dtype, int head_dim, int block_size) {
   return g.smem_bytes <= kMaxSmem;
 }
 
+bool decode_fp8_supported(pkv_dtype dtype, int head_dim, int block_size) {
+  return (dtype == PKV_BF16 || dtype == PKV_F16) && head_dim == 128 &&
+         (block_size == 16 || block_size == 32 || block_size == 64);
+}
+
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0) return PKV_OK;
-  const bool tc = decode_uses_tensor_cores(a.dtype, a.head_dim, a.block_size);
+  if (a.kv_fp8 && !decode_fp8_supported(a.dtype, a.head_dim, a.block_size))
+    return PKV_EUNSUPPORTED;
+  const bool tc = a.kv_fp8 || decode_uses_tensor_cores(a.dtype, a.head_dim, a.block_size);
   const int D = a.head_dim, BS = a.block_size;
   const WorkspaceLayout wl = workspace_layout(a.num_seqs, a.num_q_heads, D, BS,
                                               a.max_blocks_per_seq, a.partition_tokens);
@@ -754,17 +964,21 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.ws_ml = reinterpret_cast<float*>(ws + wl.ml_offset);
     P.ws_cnt = reinterpret_cast<unsigned*>(ws + wl.cnt_offset);
   }
-  const Geometry g = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts);
+  P.pair = (a.kv_fp8 && BS == 16) ? 2 : 1;
+  const Geometry g = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
+                              P.pair);
   if (g.smem_bytes > kMaxSmem) return PKV_EUNSUPPORTED;
   P.stages = g.stages;
   P.tile_bytes = g.tile_bytes;
   P.tile_stride = g.tile_stride;
   P.stage_bytes = g.stage_bytes;
   P.ring_bytes = g.ring_bytes;
-  P.boxes = tc ? D / 64 : 1;
-  P.box_cols = tc ? 64 : D;
+  P.boxes = a.kv_fp8 ? 1 : (tc ? D / 64 : 1);
+  P.box_cols = a.kv_fp8 ? D : (tc ? 64 : D);
   P.box_bytes = tc ? BS * 128 : g.tile_bytes;
-  P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  const double k_scale = a.kv_fp8 ? static_cast<double>(a.k_scale) : 1.0;
+  P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * k_scale * 1.4426950408889634);
+  P.out_scale = a.kv_fp8 ? a.v_scale : 1.f;
 
   const long long grid = static_cast<long long>(a.num_seqs) * wl.max_parts * a.num_kv_heads *
                          P.num_chunks;
@@ -772,11 +986,15 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
 
   CUtensorMap kmap, vmap;
   const long long rows = static_cast<long long>(a.num_blocks) * BS;
-  if (!make_cache_map(&kmap, a.k_cache, a.dtype, a.num_kv_heads, D, rows, P.box_cols, BS, tc) ||
-      !make_cache_map(&vmap, a.v_cache, a.dtype, a.num_kv_heads, D, rows, P.box_cols, BS, tc))
+  if (!make_cache_map(&kmap, a.k_cache, a.dtype, a.kv_fp8, a.num_kv_heads, D, rows, P.box_cols,
+                      BS, tc) ||
+      !make_cache_map(&vmap, a.v_cache, a.dtype, a.kv_fp8, a.num_kv_heads, D, rows, P.box_cols,
+                      BS, tc))
     return PKV_ECUDA;
 
-  KernelFn fn = kernel_for(a.dtype, D, BS, tc);
+  KernelFn fn = a.kv_fp8 ? (a.dtype == PKV_BF16 ? fp8_kernel_for<__nv_bfloat16>(BS)
+                                                : fp8_kernel_for<__half>(BS))
+                         : kernel_for(a.dtype, D, BS, tc);
   if (!fn) return PKV_EUNSUPPORTED;
   // the partition tickets count up from zero in every call
   if (wl.total > 0 &&

@@ -159,6 +159,41 @@ struct Mma<__half> {
   }
 };
 
+// Two E4M3 codes (low byte first) -> two fp16 values (low half first).  Exact: every
+// E4M3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(out)
+      : "r"(two_codes));
+  return out;
+}
+
+// Four E4M3 codes (byte 0 lowest) -> fp16 pairs (bytes 0,1) and (bytes 2,3).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo,
+                                                  uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
+}
+
+// Warp-wide transpose of an 8x8 matrix of 16-bit elements held as mma fragments (thread t
+// holds row t/4, columns 2(t%4) and 2(t%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t frag) {
+  uint32_t out;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(out) : "r"(frag));
+  return out;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // ---- element conversion -------------------------------------------------------------------
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

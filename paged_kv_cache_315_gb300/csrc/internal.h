@@ -28,6 +28,8 @@ struct DecodeArgs {
   void* workspace;
   size_t workspace_bytes;
   unsigned* err;  // device error word
+  bool kv_fp8;    // caches hold E4M3 codes (then k_scale / v_scale apply)
+  float k_scale, v_scale;
 };
 
 // Resolved partition size in tokens, or -1 if `partition_size` is not acceptable.
@@ -48,7 +50,15 @@ bool decode_uses_tensor_cores(pkv_dtype dtype, int head_dim, int block_size);
 // Whether any decode path serves this shape.
 bool decode_supported(pkv_dtype dtype, int head_dim, int block_size);
 
+// Whether the fp8-cache decode serves this q/out type and shape.
+bool decode_fp8_supported(pkv_dtype dtype, int head_dim, int block_size);
+
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+int launch_kv_cache_write_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                              const int64_t* slot_mapping, int num_tokens, int row_elems,
+                              pkv_dtype src_dtype, long long num_rows, float k_scale,
+                              float v_scale, unsigned* err, cudaStream_t stream);
 
 int launch_kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
                           const int64_t* slot_mapping, int num_tokens, size_t row_bytes,

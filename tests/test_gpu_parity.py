@@ -444,3 +444,94 @@ def test_swap_flags_ids_outside_either_pool(pkv):
     pkv.kv_swap_blocks(host, dev, torch.tensor([[3, 1], [0, 2], [9, 0]], device="cuda"))
     assert pkv.pkv_device_error() == pkv.PKV_DERR_PAIR
     assert torch.equal(host[1], dev[3].cpu()) and host[0].eq(0).all()
+
+
+# ------------------------------------------------------------------------------------------
+# fp8 (E4M3) caches
+# ------------------------------------------------------------------------------------------
+
+def _fp8_setup(w, ks, vs):
+    k8, v8 = synth.fp8_kv(w, ks, vs)
+    t = synth.to_torch(w, "cuda")
+    t["k8"] = torch.from_numpy(k8).cuda()
+    t["v8"] = torch.from_numpy(v8).cuda()
+    return k8, v8, t
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,bs,part", [("bf16", 8, 8, 16, 0), ("bf16", 64, 8, 16, 256),
+                                                   ("f16", 32, 8, 32, 512), ("bf16", 12, 2, 64, 128),
+                                                   ("bf16", 40, 2, 16, 512)])
+def test_fp8_decode_matches_oracle(pkv, dtype, Hq, Hkv, bs, part):
+    lens = [1, bs - 1, bs, bs + 1, 5 * bs + 3, 333, 1000, 0, 2 * bs]
+    w = synth.make_workload("f8", seed=31 + Hq + bs, dtype=dtype, context_lens=lens,
+                            num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128, block_size=bs,
+                            partition_size=part, key_outlier_frac=0.02)
+    ks, vs = 0.0625, 0.03
+    k8, v8, t = _fp8_setup(w, ks, vs)
+    out = torch.empty_like(t["q"])
+    pkv.paged_attn_decode_fp8(out, t["q"], t["k8"], t["v8"], t["block_tables"], t["context_lens"],
+                              w.scale, ks, vs, partition_size=part)
+    assert pkv.pkv_device_error() == 0
+    ref = oracle.paged_decode_fp8kv(w.q, k8, v8, w.block_tables, w.context_lens, w.scale, ks, vs,
+                                    dtype)
+    assert_close(host_out(out), ref, dtype, f"fp8 {dtype} Hq{Hq} Hkv{Hkv} bs{bs} P{part}")
+    assert (host_out(out)[7] == 0).all()
+
+
+def test_fp8_poisoned_dead_slots_are_never_read(pkv):
+    w = synth.make_workload("f8n", seed=33, dtype="bf16", context_lens=[1, 13, 17, 301],
+                            num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                            pool_slack=0.5, partition_size=64, table_pad=2 ** 30)
+    k8, v8, t = _fp8_setup(w, 0.05, 0.05)
+    out = torch.empty_like(t["q"])
+    pkv.paged_attn_decode_fp8(out, t["q"], t["k8"], t["v8"], t["block_tables"], t["context_lens"],
+                              w.scale, 0.05, 0.05, partition_size=64)
+    dead = torch.from_numpy(~synth.live_slot_mask(w)).cuda()
+    t["k8"][dead] = 0x7F     # E4M3 NaN
+    t["v8"][dead] = 0x7F
+    out2 = torch.empty_like(out)
+    pkv.paged_attn_decode_fp8(out2, t["q"], t["k8"], t["v8"], t["block_tables"], t["context_lens"],
+                              w.scale, 0.05, 0.05, partition_size=64)
+    assert pkv.pkv_device_error() == 0
+    assert torch.isfinite(out2.float()).all() and torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_fp8_slot_write_bit_exact(pkv, dtype):
+    NB, bs, Hkv, D = 20, 16, 8, 128
+    rng = np.random.default_rng(6)
+    n = 29
+    slots = rng.choice(NB * bs, size=n, replace=False).astype(np.int64)
+    slots[[2, 9]] = -1
+    k_new = synth.to_storage(rng.standard_normal((n, Hkv, D)) * 4, dtype)
+    v_new = synth.to_storage(rng.standard_normal((n, Hkv, D)) * 4, dtype)
+    k_new[0, 0, :4] = synth.to_storage(np.array([6e4, -6e4, 0.0, -0.0]), dtype)  # saturation
+    kc = np.full((NB, bs, Hkv, D), 0x11, np.uint8)
+    vc = kc.copy()
+    tk, tv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    ks, vs = 0.0371, 0.0529
+    pkv.kv_cache_write_fp8(synth.storage_to_torch(k_new, dtype, "cuda"),
+                           synth.storage_to_torch(v_new, dtype, "cuda"), tk, tv,
+                           torch.from_numpy(slots).cuda(), ks, vs)
+    assert pkv.pkv_device_error() == 0
+    assert oracle.kv_cache_write_fp8(k_new, v_new, kc, vc, slots, ks, vs, dtype) == 0
+    assert np.array_equal(tk.cpu().numpy(), kc)
+    assert np.array_equal(tv.cpu().numpy(), vc)
+
+
+def test_fp8_config3_gqa_full_size(pkv):
+    """The 70B-like GQA batch with fp8 caches: slot write of the new tokens, then decode."""
+    w = synth.config_workload(3)
+    ks, vs = 0.0625, 0.0625
+    k8, v8, t = _fp8_setup(w, ks, vs)
+    pkv.kv_cache_write_fp8(t["k_new"], t["v_new"], t["k8"], t["v8"], t["slot_mapping"], ks, vs)
+    out = torch.empty_like(t["q"])
+    pkv.paged_attn_decode_fp8(out, t["q"], t["k8"], t["v8"], t["block_tables"], t["context_lens"],
+                              w.scale, ks, vs)
+    assert pkv.pkv_device_error() == 0
+    assert oracle.kv_cache_write_fp8(w.k_new, w.v_new, k8, v8, w.slot_mapping, ks, vs, "bf16") == 0
+    assert np.array_equal(t["k8"].cpu().numpy(), k8)
+    seqs = _sample(w, 16, 8)
+    ref = oracle.paged_decode_fp8kv(w.q[seqs], k8, v8, w.block_tables[seqs], w.context_lens[seqs],
+                                    w.scale, ks, vs, "bf16")
+    assert_close(host_out(out)[seqs], ref, "bf16", "fp8 config 3")
