@@ -62,6 +62,9 @@ struct Params {
   int tile_stride;  // tile_bytes rounded up to 1024: V tile offset inside a stage
   int stage_bytes, box_bytes, box_cols, boxes, ring_bytes;
   int pair;         // physical blocks per staged tile (2 pairs 16-token blocks for fp8)
+  int ppc;          // partitions per CTA: streamed back to back, one partial each
+  int max_groups;   // CTAs per (sequence, KV head, head chunk) = ceil(max_parts / ppc)
+  int merge_off;    // byte offset of the merge buffer from the ring (0: the ring itself)
   float scale_log2;
   float out_scale;  // multiplies every output (the V scale of fp8 caches, else 1)
 };
@@ -73,6 +76,7 @@ struct Work {
   int nblk;       // blocks in the partition
   int tok_valid;  // tokens of the partition that are live
   int h0, hc;     // first query head and number of heads of this CTA
+  int nparts;     // partitions this CTA covers, starting at p
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -100,12 +104,13 @@ __device__ bool decode_work(const Params& P, int D, Work& w, int& spec_id) {
   bid /= P.num_chunks;
   w.g = static_cast<int>(bid % P.num_kv_heads);
   bid /= P.num_kv_heads;
-  w.p = static_cast<int>(bid % P.max_parts);
-  w.s = static_cast<int>(bid / P.max_parts);
+  w.p = static_cast<int>(bid % P.max_groups) * P.ppc;
+  w.s = static_cast<int>(bid / P.max_groups);
   w.h0 = w.g * P.group + w.c * P.head_chunk;
   w.hc = min(P.head_chunk, P.group - w.c * P.head_chunk);
   const int jb = w.p * P.partition_blocks + static_cast<int>(threadIdx.x);
-  spec_id = (static_cast<int>(threadIdx.x) < P.partition_blocks && jb < P.max_blocks_per_seq)
+  spec_id = (static_cast<int>(threadIdx.x) < P.partition_blocks * P.ppc &&
+             jb < P.max_blocks_per_seq)
                 ? __ldg(&P.block_tables[static_cast<size_t>(w.s) * P.max_blocks_per_seq + jb])
                 : -1;
   int L = P.context_lens[w.s];
@@ -124,13 +129,15 @@ __device__ bool decode_work(const Params& P, int D, Work& w, int& spec_id) {
     return false;
   }
   if (w.p >= w.np) return false;
+  w.nparts = min(P.ppc, w.np - w.p);
   w.blk0 = w.p * P.partition_blocks;
-  w.tok_valid = min(ptok, L - w.p * ptok);
+  w.tok_valid = min(P.ppc * ptok, L - w.p * ptok);
   w.nblk = (w.tok_valid + P.block_size - 1) / P.block_size;
   return true;
 }
 
 struct Smem {
+  float* merge;  // [kWarps][head_chunk][D] o, then [kWarps][head_chunk][2] (m, l), then weights
   uint8_t* ring;
   uint64_t* bars;
   int* ycoord;
@@ -143,7 +150,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const Params& P) {
   s.ring = raw + ((1024u - (a & 1023u)) & 1023u);
   s.bars = reinterpret_cast<uint64_t*>(s.ring + P.ring_bytes);
   s.ycoord = reinterpret_cast<int*>(s.bars + P.stages);
-  s.flags = s.ycoord + P.partition_blocks;
+  s.flags = s.ycoord + P.partition_blocks * P.ppc;
+  s.merge = reinterpret_cast<float*>(s.ring + P.merge_off);
   return s;
 }
 
@@ -248,17 +256,21 @@ __device__ void finish(const Params& P, const Work& w, int D, int HC, const floa
     }
   }
   if (!split) return;
-  __threadfence();
+  // The barrier orders every thread's partial writes before thread 0's fence, which makes
+  // them visible GPU-wide before its ticket; the CTA that draws the last ticket fences
+  // after the atomic before any thread reads the other partitions' partials.
   __syncthreads();
   if (tid == 0) {
     unsigned* cnt =
         P.ws_cnt + (static_cast<size_t>(w.s) * P.num_kv_heads + w.g) * P.num_chunks + w.c;
+    __threadfence();
     const unsigned prev = atomicAdd(cnt, 1u);
-    flags[1] = prev == static_cast<unsigned>(w.np - 1);
+    const int last = prev == static_cast<unsigned>(w.np - 1);
+    if (last) __threadfence();
+    flags[1] = last;
   }
   __syncthreads();
   if (!flags[1]) return;
-  __threadfence();
   const int warp = tid >> 5, lane = tid & 31;
   for (int r = warp; r < w.hc; r += kWarps) {
     const size_t base = (static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r) * P.max_parts;
@@ -443,63 +455,75 @@ __global__ void __launch_bounds__(kThreads)
           r0 + 8 < w.hc ? __ldg(reinterpret_cast<const uint32_t*>(qs + (r0 + 8) * D + c0 + 8)) : 0u;
     }
   }
+  // The CTA covers w.nparts consecutive partitions; the ring streams across them and each
+  // partition's state is merged and written on its own.
+  bool dead = false;  // a wait of this warp timed out: the call's output is void
   float o[D / 8][4];
+  float m[2], l[2];
+  for (int k = 0; k < w.nparts; ++k) {
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-  for (int j = warp; j < w.nblk; j += kWarps) {
-    const int st = j % P.stages;
-    if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (j / P.stages) & 1)) {
-      if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
-      drain_after_timeout(P, w, sm, j);
-      break;
-    }
-    uint8_t* ktile = sm.ring + st * P.stage_bytes;
-    uint8_t* vtile = ktile + P.tile_stride;
-    const int valid = min(BS, w.tok_valid - j * BS);
-    if (valid < BS) {
-      zero_tail_rows<D, BS>(vtile, valid, lane);
-      fence_proxy_async_smem();  // generic writes before the stage's next TMA fill
+    for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+    const int je = min(w.nblk, (k + 1) * P.partition_blocks);
+    for (int j = k * P.partition_blocks + warp; j < je && !dead; j += kWarps) {
+      const int st = j % P.stages;
+      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (j / P.stages) & 1)) {
+        if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
+        drain_after_timeout(P, w, sm, j);
+        dead = true;
+        break;
+      }
+      uint8_t* ktile = sm.ring + st * P.stage_bytes;
+      uint8_t* vtile = ktile + P.tile_stride;
+      const int valid = min(BS, w.tok_valid - j * BS);
+      if (valid < BS) {
+        zero_tail_rows<D, BS>(vtile, valid, lane);
+        fence_proxy_async_smem();  // generic writes before the stage's next TMA fill
+        __syncwarp();
+      }
+      tc_block<T, D, BS>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
       __syncwarp();
+      if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0, w.nblk);
     }
-    tc_block<T, D, BS>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
-    __syncwarp();
-    if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0, w.nblk);
-  }
 
-  __syncthreads();  // all stages consumed: the ring becomes the merge buffer
-  float* O_s = reinterpret_cast<float*>(sm.ring);
-  float* ml_s = O_s + kWarps * kTcHeads * D;
-  float* wts = ml_s + kWarps * kTcHeads * 2;
-  {
-    const int r0 = lane >> 2;
+    __syncthreads();  // every warp is done with partition k (and, with one partition, the ring)
+    const int HC = P.head_chunk;
+    float* O_s = sm.merge;
+    float* ml_s = O_s + kWarps * HC * D;
+    float* wts = ml_s + kWarps * HC * 2;
+    {
+      const int r0 = lane >> 2;
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) {
-      const int col = nd * 8 + (lane & 3) * 2;
-      if (r0 < w.hc)
-        *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0) * D + col]) = make_float2(o[nd][0], o[nd][1]);
-      if (r0 + 8 < w.hc)
-        *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0 + 8) * D + col]) =
-            make_float2(o[nd][2], o[nd][3]);
-    }
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
-    if ((lane & 3) == 0) {
-      if (r0 < w.hc) {
-        ml_s[(warp * kTcHeads + r0) * 2] = m[0];
-        ml_s[(warp * kTcHeads + r0) * 2 + 1] = l[0];
+      for (int nd = 0; nd < D / 8; ++nd) {
+        const int col = nd * 8 + (lane & 3) * 2;
+        if (r0 < w.hc)
+          *reinterpret_cast<float2*>(&O_s[(warp * HC + r0) * D + col]) = make_float2(o[nd][0], o[nd][1]);
+        if (r0 + 8 < w.hc)
+          *reinterpret_cast<float2*>(&O_s[(warp * HC + r0 + 8) * D + col]) =
+              make_float2(o[nd][2], o[nd][3]);
       }
-      if (r0 + 8 < w.hc) {
-        ml_s[(warp * kTcHeads + r0 + 8) * 2] = m[1];
-        ml_s[(warp * kTcHeads + r0 + 8) * 2 + 1] = l[1];
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+      if ((lane & 3) == 0) {
+        if (r0 < w.hc) {
+          ml_s[(warp * HC + r0) * 2] = m[0];
+          ml_s[(warp * HC + r0) * 2 + 1] = l[0];
+        }
+        if (r0 + 8 < w.hc) {
+          ml_s[(warp * HC + r0 + 8) * 2] = m[1];
+          ml_s[(warp * HC + r0 + 8) * 2 + 1] = l[1];
+        }
       }
     }
+    __syncthreads();
+    Work wk = w;
+    wk.p = w.p + k;
+    finish<T>(P, wk, D, HC, O_s, ml_s, wts, sm.flags);
+    if (k + 1 < w.nparts) __syncthreads();  // the merge buffer is read before it is reused
   }
-  __syncthreads();
-  finish<T>(P, w, D, kTcHeads, O_s, ml_s, wts, sm.flags);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -600,65 +624,76 @@ __global__ void __launch_bounds__(kThreads)
       qa[kk][3] = ld(r0 + 8, d0 + 2);
     }
   }
-  float o[16][4];
-#pragma unroll
-  for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
   constexpr int TR = BS * PAIR;  // token rows of a staged tile
   const int nv = (w.nblk + PAIR - 1) / PAIR;
-  for (int v = warp; v < nv; v += kWarps) {
-    const int st = v % P.stages;
-    if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (v / P.stages) & 1)) {
-      if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
-      drain_after_timeout(P, w, sm, v);
-      break;
-    }
-    uint8_t* ktile = sm.ring + st * P.stage_bytes;
-    uint8_t* vtile = ktile + P.tile_stride;
-    const int valid = min(TR, w.tok_valid - v * TR);
-    if (valid < TR) {
-      zero_tail_rows<64, TR>(vtile, valid, lane);  // 128-byte rows, one box
-      fence_proxy_async_smem();
-      __syncwarp();
-    }
-    fp8_block<TR>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
-    __syncwarp();
-    if (lane == 0 && v + P.stages < nv) issue_tile(P, sm, &kmap, &vmap, v + P.stages, x0, w.nblk);
-  }
-
-  __syncthreads();
-  float* O_s = reinterpret_cast<float*>(sm.ring);
-  float* ml_s = O_s + kWarps * kTcHeads * D;
-  float* wts = ml_s + kWarps * kTcHeads * 2;
-  {
-    const int r0 = lane >> 2, c = lane & 3;
+  const int vpp = P.partition_blocks / PAIR;  // staged tiles per partition
+  bool dead = false;
+  float o[16][4];
+  float m[2], l[2];
+  for (int k = 0; k < w.nparts; ++k) {
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      const int col = 32 * c + 2 * nd;
-      if (r0 < w.hc)
-        *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0) * D + col]) = make_float2(o[nd][0], o[nd][1]);
-      if (r0 + 8 < w.hc)
-        *reinterpret_cast<float2*>(&O_s[(warp * kTcHeads + r0 + 8) * D + col]) =
-            make_float2(o[nd][2], o[nd][3]);
-    }
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
-    l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
-    l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
-    if ((lane & 3) == 0) {
-      if (r0 < w.hc) {
-        ml_s[(warp * kTcHeads + r0) * 2] = m[0];
-        ml_s[(warp * kTcHeads + r0) * 2 + 1] = l[0];
+    for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+    const int ve = min(nv, (k + 1) * vpp);
+    for (int v = k * vpp + warp; v < ve && !dead; v += kWarps) {
+      const int st = v % P.stages;
+      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (v / P.stages) & 1)) {
+        if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
+        drain_after_timeout(P, w, sm, v);
+        dead = true;
+        break;
       }
-      if (r0 + 8 < w.hc) {
-        ml_s[(warp * kTcHeads + r0 + 8) * 2] = m[1];
-        ml_s[(warp * kTcHeads + r0 + 8) * 2 + 1] = l[1];
+      uint8_t* ktile = sm.ring + st * P.stage_bytes;
+      uint8_t* vtile = ktile + P.tile_stride;
+      const int valid = min(TR, w.tok_valid - v * TR);
+      if (valid < TR) {
+        zero_tail_rows<64, TR>(vtile, valid, lane);  // 128-byte rows, one box
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      fp8_block<TR>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
+      __syncwarp();
+      if (lane == 0 && v + P.stages < nv) issue_tile(P, sm, &kmap, &vmap, v + P.stages, x0, w.nblk);
+    }
+
+    __syncthreads();
+    const int HC = P.head_chunk;
+    float* O_s = sm.merge;
+    float* ml_s = O_s + kWarps * HC * D;
+    float* wts = ml_s + kWarps * HC * 2;
+    {
+      const int r0 = lane >> 2, c = lane & 3;
+#pragma unroll
+      for (int nd = 0; nd < 16; ++nd) {
+        const int col = 32 * c + 2 * nd;
+        if (r0 < w.hc)
+          *reinterpret_cast<float2*>(&O_s[(warp * HC + r0) * D + col]) = make_float2(o[nd][0], o[nd][1]);
+        if (r0 + 8 < w.hc)
+          *reinterpret_cast<float2*>(&O_s[(warp * HC + r0 + 8) * D + col]) =
+              make_float2(o[nd][2], o[nd][3]);
+      }
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
+      l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
+      if ((lane & 3) == 0) {
+        if (r0 < w.hc) {
+          ml_s[(warp * HC + r0) * 2] = m[0];
+          ml_s[(warp * HC + r0) * 2 + 1] = l[0];
+        }
+        if (r0 + 8 < w.hc) {
+          ml_s[(warp * HC + r0 + 8) * 2] = m[1];
+          ml_s[(warp * HC + r0 + 8) * 2 + 1] = l[1];
+        }
       }
     }
+    __syncthreads();
+    Work wk = w;
+    wk.p = w.p + k;
+    finish<T>(P, wk, D, HC, O_s, ml_s, wts, sm.flags);
+    if (k + 1 < w.nparts) __syncthreads();
   }
-  __syncthreads();
-  finish<T>(P, w, D, kTcHeads, O_s, ml_s, wts, sm.flags);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -737,7 +772,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   __syncthreads();
-  float* O_s = reinterpret_cast<float*>(sm.ring);
+  float* O_s = sm.merge;
   float* ml_s = O_s + kWarps * HC * D;
   float* wts = ml_s + kWarps * HC * 2;
 #pragma unroll
@@ -848,11 +883,11 @@ KernelFn kernel_for(pkv_dtype dt, int D, int BS, bool tc) {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Geometry {
-  int stages, tile_bytes, tile_stride, stage_bytes, ring_bytes, smem_bytes;
+  int stages, tile_bytes, tile_stride, stage_bytes, ring_bytes, merge_off, smem_bytes;
 };
 
 Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, int max_parts,
-                  bool fp8 = false, int pair = 1) {
+                  bool fp8 = false, int pair = 1, int ppc = 1, int head_chunk = 0) {
   Geometry g{};
   g.tile_bytes = BS * D * (fp8 ? 1 : static_cast<int>(dtype_size(dt)));
   g.tile_stride = static_cast<int>(align_up(static_cast<size_t>(pair) * g.tile_bytes, 1024));
@@ -862,9 +897,19 @@ Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, in
   const int HC = tc ? kTcHeads : kSimtHeads;
   const size_t epi = (static_cast<size_t>(kWarps) * HC * D + kWarps * HC * 2 +
                       static_cast<size_t>(HC) * max_parts) * sizeof(float);
-  g.ring_bytes = static_cast<int>(
-      align_up(std::max(static_cast<size_t>(g.stages) * g.stage_bytes, epi), 1024));
-  g.smem_bytes = 1024 + g.ring_bytes + 8 * g.stages + 4 * partition_blocks + 16;
+  if (ppc == 1) {
+    // the merge runs once, after the last tile: it reuses the ring
+    g.ring_bytes = static_cast<int>(
+        align_up(std::max(static_cast<size_t>(g.stages) * g.stage_bytes, epi), 1024));
+    g.merge_off = 0;
+  } else {
+    // a partition is merged while the next one's tiles stream in: a buffer of its own
+    const size_t merge = (static_cast<size_t>(kWarps) * head_chunk * D + kWarps * head_chunk * 2 +
+                          static_cast<size_t>(head_chunk) * max_parts) * sizeof(float);
+    g.merge_off = static_cast<int>(align_up(static_cast<size_t>(g.stages) * g.stage_bytes, 1024));
+    g.ring_bytes = static_cast<int>(align_up(g.merge_off + merge, 128));
+  }
+  g.smem_bytes = 1024 + g.ring_bytes + 8 * g.stages + 4 * partition_blocks * ppc + 16;
   return g;
 }
 
@@ -965,8 +1010,19 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.ws_cnt = reinterpret_cast<unsigned*>(ws + wl.cnt_offset);
   }
   P.pair = (a.kv_fp8 && BS == 16) ? 2 : 1;
+  // Short partitions on the tensor-core paths: a CTA streams two of them back to back
+  // (one partial each) when its merge buffer still lets three CTAs share an SM.
+  P.ppc = 1;
+  if (tc && a.partition_tokens < 1024 && P.head_chunk <= 4 && wl.max_parts > 1 &&
+      P.partition_blocks % (4 * P.pair) == 0) {
+    const Geometry g2 = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
+                                 P.pair, 2, P.head_chunk);
+    if (3 * (g2.smem_bytes + 1024) <= 228 * 1024) P.ppc = 2;
+  }
+  P.max_groups = (wl.max_parts + P.ppc - 1) / P.ppc;
   const Geometry g = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
-                              P.pair);
+                              P.pair, P.ppc, P.head_chunk);
+  P.merge_off = g.merge_off;
   if (g.smem_bytes > kMaxSmem) return PKV_EUNSUPPORTED;
   P.stages = g.stages;
   P.tile_bytes = g.tile_bytes;
@@ -980,7 +1036,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * k_scale * 1.4426950408889634);
   P.out_scale = a.kv_fp8 ? a.v_scale : 1.f;
 
-  const long long grid = static_cast<long long>(a.num_seqs) * wl.max_parts * a.num_kv_heads *
+  const long long grid = static_cast<long long>(a.num_seqs) * P.max_groups * a.num_kv_heads *
                          P.num_chunks;
   if (grid > INT_MAX) return PKV_EUNSUPPORTED;
 

@@ -163,6 +163,43 @@ def test_decode_matches_oracle(pkv, dtype, Hq, Hkv, D, bs, part):
     assert (host_out(out)[7] == 0).all()  # empty context
 
 
+# Partitions of at most 512 tokens with at most 4 query heads per KV head: one CTA streams
+# two consecutive partitions and writes a partial for each.  Lengths end on, before and
+# after partition edges so that CTAs see one or two live partitions and ragged tails.
+PAIRED_LENS = [1, 511, 512, 513, 1024, 1025, 1543, 2048, 2660, 0, 3000, 257]
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,bs,part", [("bf16", 4, 4, 16, 512), ("bf16", 16, 8, 32, 512),
+                                                   ("f16", 32, 8, 16, 256), ("bf16", 8, 2, 64, 512),
+                                                   ("bf16", 12, 4, 16, 384)])
+def test_two_partitions_per_cta_match_oracle(pkv, dtype, Hq, Hkv, bs, part):
+    w = synth.make_workload("pp", seed=50 + Hq + bs + part, dtype=dtype, context_lens=PAIRED_LENS,
+                            num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128, block_size=bs,
+                            partition_size=part, key_outlier_frac=0.02)
+    t = synth.to_torch(w, "cuda")
+    out = gpu_decode(pkv, w, t)
+    assert pkv.pkv_device_error() == 0
+    assert_close(host_out(out), oracle_decode(w), dtype, f"{dtype} Hq{Hq} Hkv{Hkv} bs{bs} P{part}")
+    assert (host_out(out)[9] == 0).all()
+
+
+@pytest.mark.parametrize("bs,part", [(16, 512), (32, 256), (64, 512)])
+def test_fp8_two_partitions_per_cta_match_oracle(pkv, bs, part):
+    w = synth.make_workload("pp8", seed=70 + bs + part, dtype="bf16", context_lens=PAIRED_LENS,
+                            num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=bs,
+                            partition_size=part, key_outlier_frac=0.02)
+    ks, vs = 0.0625, 0.03
+    k8, v8, t = _fp8_setup(w, ks, vs)
+    out = torch.empty_like(t["q"])
+    pkv.paged_attn_decode_fp8(out, t["q"], t["k8"], t["v8"], t["block_tables"], t["context_lens"],
+                              w.scale, ks, vs, partition_size=part)
+    assert pkv.pkv_device_error() == 0
+    ref = oracle.paged_decode_fp8kv(w.q, k8, v8, w.block_tables, w.context_lens, w.scale, ks, vs,
+                                    "bf16")
+    assert_close(host_out(out), ref, "bf16", f"fp8 bs{bs} P{part}")
+    assert (host_out(out)[9] == 0).all()
+
+
 def test_config1_tiny_fp32(pkv):
     w = synth.config_workload(1)
     t = synth.to_torch(w, "cuda")
