@@ -316,7 +316,11 @@ def run_ours(args) -> None:
         if ev is not None:
             ev[1].record()
 
-    launches_per_step = (2 if has_pairs else 0) + 1 + 1
+    # copies (K and V), the slot write, the decode kernel and, when the batch splits contexts
+    # (workspace in use), the one-CTA prep kernel before it (the batches here stay far below
+    # its 65536-item limit)
+    split = ws is not None and ws.numel() > 0
+    launches_per_step = (2 if has_pairs else 0) + 1 + 1 + (1 if split else 0)
     assert pkv.pkv_device_error() == 0
     for _ in range(args.warmup):
         step(t)

@@ -102,9 +102,11 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
  *                length).  paged_attn_decode_workspace_size makes the same choice.
  *   workspace    device scratch of at least paged_attn_decode_workspace_size() bytes
  *                (may be NULL when that size is 0), 16-byte aligned.  Its contents need
- *                not be initialised: each call clears the part it needs (an asynchronous
- *                memset on `stream`) before its kernel runs.  Calls that may run
- *                concurrently must not share a workspace.
+ *                not be initialised: each call first runs, on `stream`, a one-CTA kernel
+ *                that clears the partition tickets and orders the work longest first
+ *                (an asynchronous memset of the tickets instead, in natural order, when
+ *                the batch has more than 65536 sequence x partition items).  Calls that
+ *                may run concurrently must not share a workspace.
  *   stream       CUDA stream to launch on.
  * Supported: head_dim in {32, 64, 128, 256} (fp32 and fp16/bf16); the tensor-core path
  * serves fp16/bf16 with head_dim 64 or 128, block_size 16, 32 or 64 and at most 16

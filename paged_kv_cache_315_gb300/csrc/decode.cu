@@ -65,6 +65,7 @@ struct Params {
   int ppc;          // partitions per CTA: streamed back to back, one partial each
   int max_groups;   // CTAs per (sequence, KV head, head chunk) = ceil(max_parts / ppc)
   int merge_off;    // byte offset of the merge buffer from the ring (0: the ring itself)
+  const int32_t* order;  // CTA work order over (sequence, partition group) items, or null
   float scale_log2;
   float out_scale;  // multiplies every output (the V scale of fp8 caches, else 1)
 };
@@ -91,9 +92,10 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Decode blockIdx into a work unit: (sequence, partition, KV head, head chunk) from
-// slowest to fastest, so the KV heads of one physical block are read by neighbouring
-// CTAs.  Returns false when the CTA has nothing to do (after writing zeros for an empty
+// Decode blockIdx into a work unit: (item, KV head, head chunk) from slowest to fastest,
+// so the KV heads of one physical block are read by neighbouring CTAs.  An item is a
+// (sequence, group of ppc partitions) pair, taken in sequence-major order or, when the
+// launch carries one, in the order decode_prep_kernel wrote.  Returns false when the CTA has nothing to do (after writing zeros for an empty
 // context).  `spec_id` receives this thread's entry of the partition's block-table row,
 // loaded before the context length is known so that the two loads overlap (an entry past
 // the context is loaded but never used).
@@ -104,8 +106,9 @@ __device__ bool decode_work(const Params& P, int D, Work& w, int& spec_id) {
   bid /= P.num_chunks;
   w.g = static_cast<int>(bid % P.num_kv_heads);
   bid /= P.num_kv_heads;
-  w.p = static_cast<int>(bid % P.max_groups) * P.ppc;
-  w.s = static_cast<int>(bid / P.max_groups);
+  const int item = P.order ? P.order[bid] : static_cast<int>(bid);
+  w.p = (item % P.max_groups) * P.ppc;
+  w.s = item / P.max_groups;
   w.h0 = w.g * P.group + w.c * P.head_chunk;
   w.hc = min(P.head_chunk, P.group - w.c * P.head_chunk);
   const int jb = w.p * P.partition_blocks + static_cast<int>(threadIdx.x);
@@ -880,6 +883,82 @@ KernelFn kernel_for(pkv_dtype dt, int D, int BS, bool tc) {
   return simt_kernel_for<__half>(D);
 }
 
+// ------------------------------------------------------------------------------------------
+// Work order for split launches
+// ------------------------------------------------------------------------------------------
+
+constexpr int kPrepThreads = 1024;
+constexpr int kMaxOrderItems = 1 << 16;  // (sequence, group) items a prep launch sorts
+constexpr int kMaxOrderBins = 2049;      // live-block counts 0 .. 2048 of a group
+
+// Live blocks of item (sequence s, group q): the blocks the CTAs of that item stream.
+__device__ __forceinline__ int item_blocks(const int32_t* context_lens, int item, int groups,
+                                           int group_tokens, int block_size, int max_len) {
+  const int s = item / groups, q = item - s * groups;
+  int L = context_lens[s];
+  L = L < 0 ? 0 : (L > max_len ? max_len : L);
+  const int t = L - q * group_tokens;
+  return t <= 0 ? 0 : min(group_tokens / block_size, (t + block_size - 1) / block_size);
+}
+
+// One CTA, run before a split decode launch on the same stream: clears the partition
+// tickets and writes `order`, the (sequence, group) items sorted by live blocks, most
+// first (a counting sort).  Dispatching the longest units first and letting the short
+// ones fill the end of the grid is longest-processing-time list scheduling: with contexts
+// of very different lengths it keeps the SMs streaming until the last wave.  Items with
+// equal counts keep no particular order; the decode results do not depend on it.
+__global__ void __launch_bounds__(kPrepThreads)
+    decode_prep_kernel(const int32_t* __restrict__ context_lens, int num_seqs, int groups,
+                       int group_tokens, int block_size, int max_len, unsigned* cnt, int n_cnt,
+                       int32_t* order) {
+  __shared__ int bins[kMaxOrderBins];
+  __shared__ int warp_tot[kPrepThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gblocks = group_tokens / block_size;
+  const int nbins = gblocks + 1;  // bin b holds the items with gblocks - b live blocks
+  const int n = num_seqs * groups;
+  for (int i = tid; i < n_cnt; i += kPrepThreads) cnt[i] = 0u;
+  for (int b = tid; b < nbins; b += kPrepThreads) bins[b] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kPrepThreads)
+    atomicAdd(&bins[gblocks - item_blocks(context_lens, i, groups, group_tokens, block_size,
+                                           max_len)], 1);
+  __syncthreads();
+  // exclusive prefix sum of the bins: each thread owns a run of `per` bins
+  const int per = (nbins + kPrepThreads - 1) / kPrepThreads;
+  const int b0 = min(nbins, tid * per), b1 = min(nbins, b0 + per);
+  int own = 0;
+  for (int b = b0; b < b1; ++b) own += bins[b];
+  int incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    warp_tot[lane] = v;
+  }
+  __syncthreads();
+  int base = incl - own + (warp > 0 ? warp_tot[warp - 1] : 0);
+  for (int b = b0; b < b1; ++b) {
+    const int c = bins[b];
+    bins[b] = base;
+    base += c;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += kPrepThreads)
+    order[atomicAdd(&bins[gblocks - item_blocks(context_lens, i, groups, group_tokens, block_size,
+                                                max_len)], 1)] = i;
+}
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Geometry {
@@ -953,7 +1032,10 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, in
   w.o_offset = 0;
   w.ml_offset = align_up(units * head_dim * sizeof(float), 256);
   w.cnt_offset = w.ml_offset + align_up(units * 2 * sizeof(float), 256);
-  w.total = w.cnt_offset + align_up(static_cast<size_t>(num_seqs) * num_q_heads * sizeof(unsigned), 256);
+  w.order_offset =
+      w.cnt_offset + align_up(static_cast<size_t>(num_seqs) * num_q_heads * sizeof(unsigned), 256);
+  w.total = w.order_offset +
+            align_up(static_cast<size_t>(num_seqs) * w.max_parts * sizeof(int32_t), 256);
   return w;
 }
 
@@ -1052,10 +1134,25 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
                                                 : fp8_kernel_for<__half>(BS))
                          : kernel_for(a.dtype, D, BS, tc);
   if (!fn) return PKV_EUNSUPPORTED;
-  // the partition tickets count up from zero in every call
-  if (wl.total > 0 &&
-      cudaMemsetAsync(P.ws_cnt, 0, wl.total - wl.cnt_offset, stream) != cudaSuccess)
-    return PKV_ECUDA;
+  // the partition tickets count up from zero in every call; the prep kernel clears them
+  // and orders the items longest first, unless the batch has too many items for its one CTA
+  if (wl.total > 0) {
+    const long long items = static_cast<long long>(a.num_seqs) * P.max_groups;
+    const int n_cnt = a.num_seqs * a.num_kv_heads * P.num_chunks;
+    const int group_tokens = P.ppc * a.partition_tokens;
+    if (items <= kMaxOrderItems && n_cnt <= kMaxOrderItems &&
+        group_tokens / BS < kMaxOrderBins) {
+      int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(a.workspace) + wl.order_offset);
+      decode_prep_kernel<<<1, kPrepThreads, 0, stream>>>(
+          a.context_lens, a.num_seqs, P.max_groups, group_tokens, BS,
+          a.max_blocks_per_seq * BS, P.ws_cnt, n_cnt, order);
+      if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
+      P.order = order;
+    } else if (cudaMemsetAsync(P.ws_cnt, 0, wl.order_offset - wl.cnt_offset, stream) !=
+               cudaSuccess) {
+      return PKV_ECUDA;
+    }
+  }
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes) != cudaSuccess)
     return PKV_ECUDA;

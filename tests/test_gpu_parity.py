@@ -200,6 +200,24 @@ def test_fp8_two_partitions_per_cta_match_oracle(pkv, bs, part):
     assert (host_out(out)[9] == 0).all()
 
 
+def test_batch_beyond_the_ordering_limit_matches_oracle(pkv):
+    # 2100 sequences x 32 partitions of 64 tokens = 67200 items: more than the one-CTA work
+    # ordering sorts, so the launch clears the tickets with a memset and keeps natural order
+    # (8 query heads per KV head: one partition per CTA)
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 256, size=2100, endpoint=True)
+    lens[::97] = 2048
+    lens[1::89] = 1000
+    w = synth.make_workload("many", seed=5, dtype="bf16", context_lens=lens, num_q_heads=8,
+                            num_kv_heads=1, head_dim=64, block_size=16, max_blocks_per_seq=128,
+                            partition_size=64)
+    t = synth.to_torch(w, "cuda")
+    out = gpu_decode(pkv, w, t)
+    assert pkv.pkv_device_error() == 0
+    seqs = np.r_[0:40, 970:1000, 2060:2100]
+    assert_close(host_out(out)[seqs], oracle_decode(w, seqs=seqs), "bf16", "67200 items")
+
+
 def test_config1_tiny_fp32(pkv):
     w = synth.config_workload(1)
     t = synth.to_torch(w, "cuda")
