@@ -317,10 +317,10 @@ def run_ours(args) -> None:
             ev[1].record()
 
     # copies (K and V), the slot write, the decode kernel and, when the batch splits contexts
-    # (workspace in use), the one-CTA prep kernel before it (the batches here stay far below
-    # its 65536-item limit)
+    # (workspace in use), the one-CTA prep kernel before it and the merge kernel after it
+    # (the batches here stay far below the prep kernel's 65536-item limit)
     split = ws is not None and ws.numel() > 0
-    launches_per_step = (2 if has_pairs else 0) + 1 + 1 + (1 if split else 0)
+    launches_per_step = (2 if has_pairs else 0) + 1 + 1 + (2 if split else 0)
     assert pkv.pkv_device_error() == 0
     for _ in range(args.warmup):
         step(t)

@@ -102,11 +102,14 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_F16 = 2 } pkv_dtype;
  *                length).  paged_attn_decode_workspace_size makes the same choice.
  *   workspace    device scratch of at least paged_attn_decode_workspace_size() bytes
  *                (may be NULL when that size is 0), 16-byte aligned.  Its contents need
- *                not be initialised: each call first runs, on `stream`, a one-CTA kernel
- *                that clears the partition tickets and orders the work longest first
- *                (an asynchronous memset of the tickets instead, in natural order, when
- *                the batch has more than 65536 sequence x partition items).  Calls that
- *                may run concurrently must not share a workspace.
+ *                not be initialised: a call writes every workspace byte before it reads
+ *                it.  Calls that may run concurrently must not share a workspace.
+ * Launches on `stream`: one decode grid when the workspace size is 0; otherwise a
+ * one-CTA kernel that orders the work longest first (left out when the batch has more
+ * than 65536 sequence x partition items), the decode grid, and a grid that merges the
+ * partitions' partial results by log-sum-exp.  The later grids use programmatic stream
+ * serialization (they may start while the grid ahead drains and wait for it on the GPU);
+ * work enqueued on `stream` afterwards still runs after all of them.
  *   stream       CUDA stream to launch on.
  * Supported: head_dim in {32, 64, 128, 256} (fp32 and fp16/bf16); the tensor-core path
  * serves fp16/bf16 with head_dim 64 or 128, block_size 16, 32 or 64 and at most 16
@@ -238,8 +241,8 @@ int kv_copy_blocks(void* cache, const int64_t* src_dst_pairs, int num_pairs, siz
  *     use paged_attn_decode with a workspace for it, or a larger partition_size.
  *   - The first call on each device looks up the scratch array's device address (once,
  *     with that device current); make that first call before any stream capture.
- *   - All calls on a device share the one array, and it keeps the last call's contents;
- *     each call clears the counters it needs (a memset on `stream`) before its kernel.
+ *   - All calls on a device share the one array, and it keeps the last call's contents
+ *     (no call depends on them: each writes what it reads first).
  *     Calls whose work can overlap on the GPU (different streams without ordering
  *     between them) race on the array and give wrong results; order them.
  * Otherwise it behaves exactly as paged_attn_decode, with the same return codes.

@@ -19,9 +19,14 @@
 // scale*log2(e)): running max m, running sum l, unnormalised output o, rescaled by
 // 2^(m_old - m_new) whenever the max grows.  The four warps' (m, l, o) are merged in
 // shared memory at the end.  Contexts longer than one partition leave (m, l, o) per
-// partition in the workspace; the last CTA of a (s, g, c) to finish -- found with an
-// atomic ticket (cleared before the launch), no waiting -- merges them by log-sum-exp and
-// writes the output.
+// partition in the workspace, and a second grid (decode_merge_kernel, one warp per query
+// head) merges them by log-sum-exp and writes the output.  Such split launches run three
+// grids: a one-CTA prep kernel that orders the work longest first, the decode grid and
+// the merge grid, the later two launched so that they start while the one ahead drains.
+//
+// With partitions of at most 1024 tokens and at most four query heads per KV head, one
+// CTA streams two consecutive partitions through its ring (still one partial each), so
+// the next partition's tiles are in flight while the previous one is merged.
 //
 // Tensor-core path (fp16/bf16, head_dim 64/128, block_size 16/32/64): S = Q.K^T and
 // O += P.V with mma.sync m16n8k16 (fp32 accumulate); up to 16 query heads form the M
@@ -53,7 +58,6 @@ struct Params {
   const int32_t* context_lens;
   float* ws_o;
   float* ws_ml;
-  unsigned* ws_cnt;
   unsigned* err;
   int num_seqs, num_q_heads, num_kv_heads, group, head_chunk, num_chunks;
   int max_blocks_per_seq, num_blocks, block_size;
@@ -101,6 +105,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 // the context is loaded but never used).
 template <typename T>
 __device__ bool decode_work(const Params& P, int D, Work& w, int& spec_id) {
+  // Launched behind the prep kernel, this grid may start before it ends: wait for it (a
+  // no-op otherwise).  Every CTA has started once all pass here, which lets the merge
+  // kernel behind this grid be scheduled into the slots the tail leaves free.
+  griddep_wait();
+  griddep_launch_dependents();
   long long bid = blockIdx.x;
   w.c = static_cast<int>(bid % P.num_chunks);
   bid /= P.num_chunks;
@@ -140,11 +149,10 @@ __device__ bool decode_work(const Params& P, int D, Work& w, int& spec_id) {
 }
 
 struct Smem {
-  float* merge;  // [kWarps][head_chunk][D] o, then [kWarps][head_chunk][2] (m, l), then weights
+  float* merge;  // [kWarps][head_chunk][D] o, then [kWarps][head_chunk][2] (m, l)
   uint8_t* ring;
   uint64_t* bars;
   int* ycoord;
-  int* flags;
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, const Params& P) {
@@ -153,7 +161,6 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const Params& P) {
   s.ring = raw + ((1024u - (a & 1023u)) & 1023u);
   s.bars = reinterpret_cast<uint64_t*>(s.ring + P.ring_bytes);
   s.ycoord = reinterpret_cast<int*>(s.bars + P.stages);
-  s.flags = s.ycoord + P.partition_blocks * P.ppc;
   s.merge = reinterpret_cast<float*>(s.ring + P.merge_off);
   return s;
 }
@@ -201,8 +208,6 @@ __device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, c
   }
   if (tid == 0) {
     for (int i = 0; i < P.stages; ++i) mbar_init(smem_addr(&sm.bars[i]), 1);
-    sm.flags[0] = 0;
-    sm.flags[1] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -223,12 +228,12 @@ __device__ __forceinline__ void drain_after_timeout(const Params& P, const Work&
     mbar_wait_bounded(smem_addr(&sm.bars[jj % P.stages]), (jj / P.stages) & 1);
 }
 
-// Merge the four warps' (m, l, o) of each query head; write the output (one partition)
-// or this partition's partials, and let the last partition CTA merge all partials.
-// O_s: [kWarps][HC][D] floats, ml_s: [kWarps][HC][2] (m in log2 units, l), wts: [HC][np].
+// Merge the four warps' (m, l, o) of each query head; write the output (a context of one
+// partition) or this partition's partial (m, l, o), which decode_merge_kernel reduces.
+// O_s: [kWarps][HC][D] floats, ml_s: [kWarps][HC][2] (m in log2 units, l).
 template <typename T>
 __device__ void finish(const Params& P, const Work& w, int D, int HC, const float* O_s,
-                       const float* ml_s, float* wts, int* flags) {
+                       const float* ml_s) {
   const int tid = threadIdx.x;
   const int n = w.hc * D;
   const bool split = w.np > 1;
@@ -257,47 +262,6 @@ __device__ void finish(const Params& P, const Work& w, int D, int HC, const floa
         P.ws_ml[idx * 2 + 1] = den;
       }
     }
-  }
-  if (!split) return;
-  // The barrier orders every thread's partial writes before thread 0's fence, which makes
-  // them visible GPU-wide before its ticket; the CTA that draws the last ticket fences
-  // after the atomic before any thread reads the other partitions' partials.
-  __syncthreads();
-  if (tid == 0) {
-    unsigned* cnt =
-        P.ws_cnt + (static_cast<size_t>(w.s) * P.num_kv_heads + w.g) * P.num_chunks + w.c;
-    __threadfence();
-    const unsigned prev = atomicAdd(cnt, 1u);
-    const int last = prev == static_cast<unsigned>(w.np - 1);
-    if (last) __threadfence();
-    flags[1] = last;
-  }
-  __syncthreads();
-  if (!flags[1]) return;
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int r = warp; r < w.hc; r += kWarps) {
-    const size_t base = (static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r) * P.max_parts;
-    float M = -INFINITY;
-    for (int p = lane; p < w.np; p += 32) M = fmaxf(M, __ldcg(&P.ws_ml[(base + p) * 2]));
-    M = warp_max(M);
-    float den = 0.f;
-    for (int p = lane; p < w.np; p += 32) {
-      const float e = exp2f(__ldcg(&P.ws_ml[(base + p) * 2]) - M);
-      wts[r * w.np + p] = e;
-      den += e * __ldcg(&P.ws_ml[(base + p) * 2 + 1]);
-    }
-    den = warp_sum(den);
-    const float inv = 1.f / den;
-    for (int p = lane; p < w.np; p += 32) wts[r * w.np + p] *= inv;
-  }
-  __syncthreads();
-  for (int i = tid; i < n; i += kThreads) {
-    const int r = i / D, d = i - r * D;
-    const size_t row = static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r;
-    const size_t base = row * P.max_parts;
-    float acc = 0.f;
-    for (int p = 0; p < w.np; ++p) acc += wts[r * w.np + p] * __ldcg(&P.ws_o[(base + p) * D + d]);
-    out[row * D + d] = from_f32<T>(acc * P.out_scale);
   }
 }
 
@@ -494,7 +458,6 @@ __global__ void __launch_bounds__(kThreads)
     const int HC = P.head_chunk;
     float* O_s = sm.merge;
     float* ml_s = O_s + kWarps * HC * D;
-    float* wts = ml_s + kWarps * HC * 2;
     {
       const int r0 = lane >> 2;
 #pragma unroll
@@ -524,7 +487,7 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     Work wk = w;
     wk.p = w.p + k;
-    finish<T>(P, wk, D, HC, O_s, ml_s, wts, sm.flags);
+    finish<T>(P, wk, D, HC, O_s, ml_s);
     if (k + 1 < w.nparts) __syncthreads();  // the merge buffer is read before it is reused
   }
 }
@@ -664,7 +627,6 @@ __global__ void __launch_bounds__(kThreads)
     const int HC = P.head_chunk;
     float* O_s = sm.merge;
     float* ml_s = O_s + kWarps * HC * D;
-    float* wts = ml_s + kWarps * HC * 2;
     {
       const int r0 = lane >> 2, c = lane & 3;
 #pragma unroll
@@ -694,7 +656,7 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     Work wk = w;
     wk.p = w.p + k;
-    finish<T>(P, wk, D, HC, O_s, ml_s, wts, sm.flags);
+    finish<T>(P, wk, D, HC, O_s, ml_s);
     if (k + 1 < w.nparts) __syncthreads();
   }
 }
@@ -777,7 +739,6 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   float* O_s = sm.merge;
   float* ml_s = O_s + kWarps * HC * D;
-  float* wts = ml_s + kWarps * HC * 2;
 #pragma unroll
   for (int h = 0; h < HC; ++h) {
     if (h < w.hc) {
@@ -790,7 +751,7 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
   __syncthreads();
-  finish<T>(P, w, D, HC, O_s, ml_s, wts, sm.flags);
+  finish<T>(P, w, D, HC, O_s, ml_s);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -901,23 +862,21 @@ __device__ __forceinline__ int item_blocks(const int32_t* context_lens, int item
   return t <= 0 ? 0 : min(group_tokens / block_size, (t + block_size - 1) / block_size);
 }
 
-// One CTA, run before a split decode launch on the same stream: clears the partition
-// tickets and writes `order`, the (sequence, group) items sorted by live blocks, most
+// One CTA, run before a split decode launch on the same stream: writes `order`, the (sequence, group) items sorted by live blocks, most
 // first (a counting sort).  Dispatching the longest units first and letting the short
 // ones fill the end of the grid is longest-processing-time list scheduling: with contexts
 // of very different lengths it keeps the SMs streaming until the last wave.  Items with
 // equal counts keep no particular order; the decode results do not depend on it.
 __global__ void __launch_bounds__(kPrepThreads)
     decode_prep_kernel(const int32_t* __restrict__ context_lens, int num_seqs, int groups,
-                       int group_tokens, int block_size, int max_len, unsigned* cnt, int n_cnt,
-                       int32_t* order) {
+                       int group_tokens, int block_size, int max_len, int32_t* order) {
+  griddep_launch_dependents();  // the decode grid may be scheduled; it waits for this one
   __shared__ int bins[kMaxOrderBins];
   __shared__ int warp_tot[kPrepThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gblocks = group_tokens / block_size;
   const int nbins = gblocks + 1;  // bin b holds the items with gblocks - b live blocks
   const int n = num_seqs * groups;
-  for (int i = tid; i < n_cnt; i += kPrepThreads) cnt[i] = 0u;
   for (int b = tid; b < nbins; b += kPrepThreads) bins[b] = 0;
   __syncthreads();
   for (int i = tid; i < n; i += kPrepThreads)
@@ -959,6 +918,100 @@ __global__ void __launch_bounds__(kPrepThreads)
                                                 max_len)], 1)] = i;
 }
 
+// ------------------------------------------------------------------------------------------
+// Reduction of the partition partials
+// ------------------------------------------------------------------------------------------
+
+constexpr int kMergeWarps = 4;
+
+// One warp per (sequence, query head) row whose context spans np > 1 partitions: the
+// log-sum-exp reduction of the partition partials (m_p in log2 units, l_p, o_p):
+//   M = max_p m_p,  w_p = 2^(m_p - M) / sum_q 2^(m_q - M) l_q,  out = sum_p w_p o_p,
+// which equals the single-pass softmax-weighted sum of values up to rounding order.
+// Rows of one partition were written by the decode kernel itself.  Launched right after
+// the decode kernel, possibly while it still runs: the partials are read only after the
+// grid dependency wait, through L2.
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Params P) {
+  constexpr int V = D / 32;  // columns per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
+  int np = 0;
+  if (row < static_cast<long long>(P.num_seqs) * P.num_q_heads) {
+    int L = P.context_lens[row / P.num_q_heads];
+    const int Lmax = P.max_blocks_per_seq * P.block_size;
+    L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
+    const int ptok = P.partition_blocks * P.block_size;
+    np = (L + ptok - 1) / ptok;
+  }
+  // every thread waits, even one with nothing to merge, so that this grid never ends
+  // before the decode grid it depends on
+  griddep_wait();
+  if (np <= 1) return;
+  const size_t base = static_cast<size_t>(row) * P.max_parts;
+  const float* ml = P.ws_ml + base * 2;
+  float M = -INFINITY;
+  for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(&ml[2 * p]));
+  M = warp_max(M);
+  float den = 0.f;
+  for (int p = lane; p < np; p += 32) den += exp2f(__ldcg(&ml[2 * p]) - M) * __ldcg(&ml[2 * p + 1]);
+  den = warp_sum(den);
+  const float inv = 1.f / den;
+  float acc[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) acc[k] = 0.f;
+  const float* o = P.ws_o + base * D + lane * V;
+  for (int p0 = 0; p0 < np; p0 += 32) {
+    const int p = p0 + lane;
+    const float wp = p < np ? exp2f(__ldcg(&ml[2 * p]) - M) * inv : 0.f;
+    const int cnt = min(32, np - p0);
+#pragma unroll 8
+    for (int i = 0; i < cnt; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, wp, i);
+      const float* src = o + static_cast<size_t>(p0 + i) * D;
+      if constexpr (V % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < V; k += 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + k));
+          acc[k] += wi * x.x;
+          acc[k + 1] += wi * x.y;
+          acc[k + 2] += wi * x.z;
+          acc[k + 3] += wi * x.w;
+        }
+      } else if constexpr (V == 2) {
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+        acc[0] += wi * x.x;
+        acc[1] += wi * x.y;
+      } else {
+        acc[0] += wi * __ldcg(src);
+      }
+    }
+  }
+  T* out = static_cast<T*>(P.out) + static_cast<size_t>(row) * D + lane * V;
+#pragma unroll
+  for (int k = 0; k < V; ++k) out[k] = from_f32<T>(acc[k] * P.out_scale);
+}
+
+using MergeFn = void (*)(const Params);
+
+template <typename T>
+MergeFn merge_kernel_for_type(int D) {
+  switch (D) {
+    case 32: return decode_merge_kernel<T, 32>;
+    case 64: return decode_merge_kernel<T, 64>;
+    case 128: return decode_merge_kernel<T, 128>;
+    case 256: return decode_merge_kernel<T, 256>;
+    default: return nullptr;
+  }
+}
+
+MergeFn merge_kernel_for(pkv_dtype dt, int D) {
+  if (dt == PKV_F32) return merge_kernel_for_type<float>(D);
+  if (dt == PKV_BF16) return merge_kernel_for_type<__nv_bfloat16>(D);
+  if (dt == PKV_F16) return merge_kernel_for_type<__half>(D);
+  return nullptr;
+}
+
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Geometry {
@@ -974,8 +1027,7 @@ Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, in
   const int per_warp = std::max(1, std::min(kMaxStageSet, 16384 / g.stage_bytes));
   g.stages = kWarps * per_warp;
   const int HC = tc ? kTcHeads : kSimtHeads;
-  const size_t epi = (static_cast<size_t>(kWarps) * HC * D + kWarps * HC * 2 +
-                      static_cast<size_t>(HC) * max_parts) * sizeof(float);
+  const size_t epi = (static_cast<size_t>(kWarps) * HC * D + kWarps * HC * 2) * sizeof(float);
   if (ppc == 1) {
     // the merge runs once, after the last tile: it reuses the ring
     g.ring_bytes = static_cast<int>(
@@ -983,12 +1035,12 @@ Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, in
     g.merge_off = 0;
   } else {
     // a partition is merged while the next one's tiles stream in: a buffer of its own
-    const size_t merge = (static_cast<size_t>(kWarps) * head_chunk * D + kWarps * head_chunk * 2 +
-                          static_cast<size_t>(head_chunk) * max_parts) * sizeof(float);
+    const size_t merge =
+        (static_cast<size_t>(kWarps) * head_chunk * D + kWarps * head_chunk * 2) * sizeof(float);
     g.merge_off = static_cast<int>(align_up(static_cast<size_t>(g.stages) * g.stage_bytes, 1024));
     g.ring_bytes = static_cast<int>(align_up(g.merge_off + merge, 128));
   }
-  g.smem_bytes = 1024 + g.ring_bytes + 8 * g.stages + 4 * partition_blocks * ppc + 16;
+  g.smem_bytes = 1024 + g.ring_bytes + 8 * g.stages + 4 * partition_blocks * ppc;
   return g;
 }
 
@@ -1031,9 +1083,7 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, in
   const size_t units = static_cast<size_t>(num_seqs) * num_q_heads * w.max_parts;
   w.o_offset = 0;
   w.ml_offset = align_up(units * head_dim * sizeof(float), 256);
-  w.cnt_offset = w.ml_offset + align_up(units * 2 * sizeof(float), 256);
-  w.order_offset =
-      w.cnt_offset + align_up(static_cast<size_t>(num_seqs) * num_q_heads * sizeof(unsigned), 256);
+  w.order_offset = w.ml_offset + align_up(units * 2 * sizeof(float), 256);
   w.total = w.order_offset +
             align_up(static_cast<size_t>(num_seqs) * w.max_parts * sizeof(int32_t), 256);
   return w;
@@ -1089,7 +1139,6 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     char* ws = static_cast<char*>(a.workspace);
     P.ws_o = reinterpret_cast<float*>(ws + wl.o_offset);
     P.ws_ml = reinterpret_cast<float*>(ws + wl.ml_offset);
-    P.ws_cnt = reinterpret_cast<unsigned*>(ws + wl.cnt_offset);
   }
   P.pair = (a.kv_fp8 && BS == 16) ? 2 : 1;
   // Short partitions on the tensor-core paths: a CTA streams two of them back to back
@@ -1134,30 +1183,54 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
                                                 : fp8_kernel_for<__half>(BS))
                          : kernel_for(a.dtype, D, BS, tc);
   if (!fn) return PKV_EUNSUPPORTED;
-  // the partition tickets count up from zero in every call; the prep kernel clears them
-  // and orders the items longest first, unless the batch has too many items for its one CTA
-  if (wl.total > 0) {
+  const bool split = wl.total > 0;
+  MergeFn merge = split ? merge_kernel_for(a.dtype, D) : nullptr;
+  if (split && !merge) return PKV_EUNSUPPORTED;
+  // Split launches: the prep kernel orders the items longest first (natural order beyond
+  // its item limit), then the decode grid, then the merge grid.  The two later grids are
+  // launched with programmatic stream serialization: they may be scheduled before the grid
+  // ahead of them ends and wait for it on the device (griddepcontrol), which hides their
+  // launch latency.
+  bool ordered = false;
+  if (split) {
     const long long items = static_cast<long long>(a.num_seqs) * P.max_groups;
-    const int n_cnt = a.num_seqs * a.num_kv_heads * P.num_chunks;
     const int group_tokens = P.ppc * a.partition_tokens;
-    if (items <= kMaxOrderItems && n_cnt <= kMaxOrderItems &&
-        group_tokens / BS < kMaxOrderBins) {
+    if (items <= kMaxOrderItems && group_tokens / BS < kMaxOrderBins) {
       int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(a.workspace) + wl.order_offset);
-      decode_prep_kernel<<<1, kPrepThreads, 0, stream>>>(
-          a.context_lens, a.num_seqs, P.max_groups, group_tokens, BS,
-          a.max_blocks_per_seq * BS, P.ws_cnt, n_cnt, order);
+      decode_prep_kernel<<<1, kPrepThreads, 0, stream>>>(a.context_lens, a.num_seqs, P.max_groups,
+                                                         group_tokens, BS,
+                                                         a.max_blocks_per_seq * BS, order);
       if (cudaGetLastError() != cudaSuccess) return PKV_ECUDA;
       P.order = order;
-    } else if (cudaMemsetAsync(P.ws_cnt, 0, wl.order_offset - wl.cnt_offset, stream) !=
-               cudaSuccess) {
-      return PKV_ECUDA;
+      ordered = true;
     }
   }
   if (cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                            cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes) != cudaSuccess)
     return PKV_ECUDA;
-  fn<<<static_cast<unsigned>(grid), kThreads, g.smem_bytes, stream>>>(kmap, vmap, P);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(g.smem_bytes);
+  cfg.stream = stream;
+  cfg.attrs = ordered ? pdl : nullptr;
+  cfg.numAttrs = ordered ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, fn, kmap, vmap, P) != cudaSuccess) return PKV_ECUDA;
+  if (split) {
+    const long long rows = static_cast<long long>(a.num_seqs) * a.num_q_heads;
+    cudaLaunchConfig_t mcfg{};
+    mcfg.gridDim = dim3(static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps));
+    mcfg.blockDim = dim3(kMergeWarps * 32);
+    mcfg.dynamicSmemBytes = 0;
+    mcfg.stream = stream;
+    mcfg.attrs = pdl;
+    mcfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&mcfg, merge, P) != cudaSuccess) return PKV_ECUDA;
+  }
+  return PKV_OK;
 }
 
 }  // namespace pkv

@@ -83,6 +83,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- programmatic dependent launch -------------------------------------------------------
+
+// Wait until the grid this one was launched behind (with programmatic stream
+// serialization) has completed and its memory operations are visible; returns at once
+// for a grid launched without that attribute.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the grid launched behind this one to be scheduled (its griddep_wait still waits
+// for this grid to complete).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- TMA ---------------------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

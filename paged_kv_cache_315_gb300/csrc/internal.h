@@ -39,7 +39,7 @@ int resolve_partition_tokens(int partition_size, int block_size, int num_seqs, i
 
 // Workspace layout shared by the size query and the launcher.
 struct WorkspaceLayout {
-  size_t o_offset, ml_offset, cnt_offset, order_offset, total;
+  size_t o_offset, ml_offset, order_offset, total;
   int max_parts;
 };
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int block_size,

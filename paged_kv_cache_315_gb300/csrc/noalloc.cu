@@ -1,7 +1,7 @@
 // noalloc.cu -- paged_attn_decode for callers that cannot allocate device memory.
 //
-// The decode kernel needs scratch memory: a work counter, one ticket per (sequence, KV
-// head) and, when a context spans several partitions, the partitions' partial results.
+// The decode kernels need scratch memory when a context spans several partitions: the
+// partitions' partial results and the work order of the decode grid.
 // paged_attn_decode takes that scratch from the caller.  Some callers have no way to
 // provide it: a host program that owns the device's whole memory budget and hands the
 // library only the tensors of a call, or a hot path on which allocating is not allowed.
@@ -66,8 +66,7 @@ extern "C" int paged_attn_decode_noalloc(void* out, const void* q, const void* k
   int err = PKV_OK;
   void* scratch = pkv::scratch_address(&err);
   if (!scratch) return err;
-  // paged_attn_decode clears the scratch's counters on `stream` before its kernel runs;
-  // the partial results need no clearing (each is written before it is read)
+  // nothing in the scratch needs clearing: every byte a call reads it wrote first
   return paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                            num_blocks, scale, dtype, partition_size, scratch,

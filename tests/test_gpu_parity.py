@@ -202,7 +202,7 @@ def test_fp8_two_partitions_per_cta_match_oracle(pkv, bs, part):
 
 def test_batch_beyond_the_ordering_limit_matches_oracle(pkv):
     # 2100 sequences x 32 partitions of 64 tokens = 67200 items: more than the one-CTA work
-    # ordering sorts, so the launch clears the tickets with a memset and keeps natural order
+    # ordering sorts, so the launch leaves the prep kernel out and keeps natural order
     # (8 query heads per KV head: one partition per CTA)
     rng = np.random.default_rng(5)
     lens = rng.integers(1, 256, size=2100, endpoint=True)
