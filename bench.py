@@ -42,14 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # beside it (profiles/ holds the captures).
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each
-    "13b-mha-b64-bf16@2048": {"bytes": 1408788480 + 3472640, "decode_cu_sha": "d951b0d02173d71c"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 964699648 + 7546624, "decode_cu_sha": "d951b0d02173d71c"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328653056 + 6000384, "decode_cu_sha": "d951b0d02173d71c"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4326800896 + 36461568, "decode_cu_sha": "d951b0d02173d71c"},
-    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704839424 + 3758336, "decode_cu_sha": "d951b0d02173d71c"},
-    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483400192 + 6973952, "decode_cu_sha": "d951b0d02173d71c"},
-    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164931840 + 4155648, "decode_cu_sha": "d951b0d02173d71c"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2162245376 + 35482112, "decode_cu_sha": "d951b0d02173d71c"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408829696 + 3771392, "decode_cu_sha": "b4833870dd0161af"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963545600 + 6620416, "decode_cu_sha": "b4833870dd0161af"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328524800 + 4629248, "decode_cu_sha": "b4833870dd0161af"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4295690240 + 35983872, "decode_cu_sha": "b4833870dd0161af"},
+    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704843008 + 3724288, "decode_cu_sha": "b4833870dd0161af"},
+    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483319296 + 5715968, "decode_cu_sha": "b4833870dd0161af"},
+    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164936448 + 4075264, "decode_cu_sha": "b4833870dd0161af"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148132352 + 34985216, "decode_cu_sha": "b4833870dd0161af"},
 }
 
 
@@ -431,8 +431,9 @@ def run_ours(args) -> None:
         "decode_ms": round(decode_ms, 5),
         "partition_tokens": part,
         "kv_dtype": "e4m3" if fp8 else w.dtype,
-        "roofline": {"kernel": "paged_attn_decode_fp8 (decode_fp8_kernel)" if fp8
-                     else "paged_attn_decode (decode_tc_kernel)", "bound": "hbm",
+        "roofline": {"kernel": ("paged_attn_decode_fp8 (decode_fp8_kernel" if fp8
+                                else "paged_attn_decode (decode_tc_kernel")
+                     + (" + prep + merge grids)" if split else ")"), "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": ab,
