@@ -1,4 +1,4 @@
-"""CPU oracle for paged decode attention, slot writes and block copies.
+"""CPU oracle for paged decode and chunked-prefill attention, slot writes and block copies.
 
 TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline / reference legs may import this package. The product
@@ -19,6 +19,7 @@ from .oracle import (  # noqa: F401
     paged_decode,
     paged_decode_fp8kv,
     paged_decode_partitioned,
+    paged_prefill,
     slot,
     swap_blocks,
 )

@@ -58,6 +58,9 @@ def _load():
         lib.pkvo_paged_decode_partitioned.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32,
                                                       i32, i32, i32, dbl, i32, i32]
         lib.pkvo_paged_decode_partitioned.restype = i32
+        lib.pkvo_paged_prefill.argtypes = [P, P, P, P, i32, P, P, P, i32, i32, i32, i32, i32,
+                                           i32, i32, i32, dbl, i32]
+        lib.pkvo_paged_prefill.restype = i32
         lib.pkvo_kv_cache_write.argtypes = [P, P, P, P, P, i32, sz, i32, i32]
         lib.pkvo_kv_cache_write.restype = i32
         lib.pkvo_copy_blocks.argtypes = [P, P, i32, sz, i32]
@@ -148,6 +151,36 @@ def paged_decode_partitioned(q, k_cache, v_cache, block_tables, context_lens, sc
         B, Hq, Hkv, D, bs, MB, NB, float(scale), int(partition_size), int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle paged_decode_partitioned rejected its inputs (code {rc})")
+    return out
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, dtype,
+                  num_threads: int = 0) -> np.ndarray:
+    """fp64 chunked-prefill attention by its definition; returns ``[T, Hq, D]`` float64.
+
+    ``q`` is ``[T, Hq, D]``; sequence s owns query rows ``query_start[s] ..
+    query_start[s+1]-1``, the last ``n`` positions of its ``context_lens[s]`` cached
+    tokens, and each row attends causally (positions ``0 .. L-n+i``).
+    """
+    q = _check_storage("q", q, dtype)
+    k_cache = _check_storage("k_cache", k_cache, dtype)
+    v_cache = _check_storage("v_cache", v_cache, dtype)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, Dk = k_cache.shape
+    if Dk != D or v_cache.shape != k_cache.shape:
+        raise ValueError("q, k_cache and v_cache disagree on head_dim or shape")
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    qs = _c(query_start, np.int32)
+    B = cl.shape[0]
+    if bt.ndim != 2 or bt.shape[0] != B or qs.shape != (B + 1,):
+        raise ValueError("block_tables / query_start do not match context_lens")
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    rc = _load().pkvo_paged_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                    DTYPE_CODES[dtype], _ptr(bt), _ptr(cl), _ptr(qs), B, T, Hq,
+                                    Hkv, D, bs, bt.shape[1], NB, float(scale), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle paged_prefill rejected its inputs (code {rc})")
     return out
 
 

@@ -41,6 +41,13 @@
  *    "Copy-on-write makes shared prefixes practical": the manager allocates a new
  *    block and copies only that block.
  *
+ *  - Chunked prefill.  "Paged Attention: How vLLM Solves the KV Cache Memory Problem",
+ *    section "Continuous Batching and Chunked Prefill": a long prompt is processed in
+ *    chunks interleaved with decode steps.  A chunk of n query tokens of a sequence whose
+ *    cache holds L tokens (the chunk's own keys and values written last) sits at
+ *    positions L-n .. L-1; query i of the chunk attends the positions 0 .. L-n+i (causal
+ *    attention, as in any prefill).  Decode is the case n = 1.
+ *
  * Layout conventions (the readings taken where the pages are silent):
  *  - cache tensors are [num_blocks, block_size, num_kv_heads, head_dim], row-major;
  *    K and V are separate tensors of the same shape;
@@ -296,6 +303,83 @@ int pkvo_paged_decode_partitioned(double* out, const void* q, const void* k_cach
         }
         for (int d = 0; d < head_dim; ++d) o[d] /= den;
         free(sc); free(mi); free(li); free(oi);
+    }
+    return failed ? PKVO_ENOMEM : PKVO_OK;
+}
+
+/* ---- chunked prefill: several query tokens per sequence, causal ------------------ */
+/*
+ * q and out are [num_q_tokens, num_q_heads, head_dim]; sequence s owns query rows
+ * query_start[s] .. query_start[s+1]-1 (query_start[0] = 0, query_start[num_seqs] =
+ * num_q_tokens, non-decreasing).  With n = query_start[s+1] - query_start[s] and
+ * L = context_lens[s] (n <= L), row query_start[s] + i, head h, is
+ *     pos   = L - n + i
+ *     s_p   = scale * <q_row,h, K_p>                   p = 0 .. pos
+ *     out   = sum_p softmax(s)_p * V_p
+ * with K_p, V_p read through sequence s's block table as for decode.
+ */
+int pkvo_paged_prefill(double* out, const void* q, const void* k_cache, const void* v_cache,
+                       int dtype, const int32_t* block_tables, const int32_t* context_lens,
+                       const int32_t* query_start, int num_seqs, int num_q_tokens,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int max_blocks_per_seq, int num_blocks, double scale, int num_threads) {
+    if (!check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                      max_blocks_per_seq, num_blocks, dtype) || num_q_tokens < 0)
+        return PKVO_EINVAL;
+    if (!check_tables(block_tables, context_lens, num_seqs, block_size, max_blocks_per_seq,
+                      num_blocks))
+        return PKVO_EINVAL;
+    if (num_seqs > 0 && (query_start[0] != 0 || query_start[num_seqs] != num_q_tokens))
+        return PKVO_EINVAL;
+    for (int s = 0; s < num_seqs; ++s) {
+        int64_t n = (int64_t)query_start[s + 1] - query_start[s];
+        if (n < 0 || n > context_lens[s]) return PKVO_EINVAL;
+    }
+    int group = num_q_heads / num_kv_heads;
+    int64_t units = (int64_t)num_q_tokens * num_q_heads;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        int64_t t = u / num_q_heads;
+        int h = (int)(u % num_q_heads);
+        int g = h / group;
+        int s = 0;
+        while (query_start[s + 1] <= t) ++s;  /* the sequence that owns query row t */
+        int64_t n = (int64_t)query_start[s + 1] - query_start[s];
+        int64_t i = t - query_start[s];
+        int64_t pos = (int64_t)context_lens[s] - n + i;
+        double* o = out + (size_t)u * head_dim;
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        const int32_t* bt_row = block_tables + (size_t)s * max_blocks_per_seq;
+        size_t qbase = ((size_t)t * num_q_heads + h) * (size_t)head_dim;
+        double* w = (double*)malloc((size_t)(pos + 1) * sizeof(double));
+        if (!w) { failed = 1; continue; }
+        double m = -INFINITY;
+        for (int64_t p = 0; p <= pos; ++p) {
+            int32_t phys, off;
+            pkvo_locate(bt_row, p, block_size, &phys, &off);
+            double dot = 0.0;
+            for (int d = 0; d < head_dim; ++d)
+                dot += elem(q, qbase + d, dtype) *
+                       elem(k_cache, cache_index(phys, off, g, d, block_size, num_kv_heads,
+                                                 head_dim), dtype);
+            w[p] = scale * dot;
+            if (w[p] > m) m = w[p];
+        }
+        double z = 0.0;
+        for (int64_t p = 0; p <= pos; ++p) { w[p] = exp(w[p] - m); z += w[p]; }
+        for (int64_t p = 0; p <= pos; ++p) {
+            int32_t phys, off;
+            pkvo_locate(bt_row, p, block_size, &phys, &off);
+            for (int d = 0; d < head_dim; ++d)
+                o[d] += w[p] * elem(v_cache, cache_index(phys, off, g, d, block_size, num_kv_heads,
+                                                         head_dim), dtype);
+        }
+        for (int d = 0; d < head_dim; ++d) o[d] /= z;
+        free(w);
     }
     return failed ? PKVO_ENOMEM : PKVO_OK;
 }

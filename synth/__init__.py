@@ -138,6 +138,10 @@ class Workload:
     slot_mapping: np.ndarray | None = None  # int64 [N]
     # copy-on-write pairs applied before the writes (kv_copy_blocks)
     copy_pairs: np.ndarray | None = None    # int64 [P, 2]
+    # chunked prefill: query rows of every sequence's chunk (the chunk's keys and values
+    # are the last n cached tokens, already in the pool)
+    chunk_q: np.ndarray | None = None       # [T, Hq, D]
+    query_start: np.ndarray | None = None   # int32 [B + 1]
     info: dict = field(default_factory=dict)
 
     @property
@@ -266,6 +270,48 @@ def add_new_tokens(w: Workload, seed: int) -> None:
     w.k_new = normal_storage(s_k, (B, Hkv, D), w.dtype)
     w.v_new = normal_storage(s_v, (B, Hkv, D), w.dtype)
     w.slot_mapping = slots
+
+
+def make_prefill_workload(name: str, *, seed: int, dtype: str, prior_lens, chunk_lens,
+                          num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                          **kw) -> Workload:
+    """Chunks of ``chunk_lens[s]`` query tokens after ``prior_lens[s]`` cached tokens.
+
+    The pool holds ``prior + chunk`` tokens per sequence (the chunk's own keys and values
+    included, as after its slot writes); ``chunk_q`` holds the chunk's query rows, packed
+    sequence after sequence, and ``query_start`` their offsets.
+    """
+    prior = np.asarray(prior_lens, dtype=np.int64)
+    chunk = np.asarray(chunk_lens, dtype=np.int64)
+    if prior.shape != chunk.shape or (prior < 0).any() or (chunk < 0).any():
+        raise ValueError("prior_lens and chunk_lens must be non-negative and of equal length")
+    w = make_workload(name, seed=seed, dtype=dtype, context_lens=(prior + chunk).astype(np.int32),
+                      num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                      block_size=block_size, **kw)
+    qs = np.zeros(len(chunk) + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(chunk)
+    s_q = np.random.SeedSequence([seed, 11])
+    w.chunk_q = normal_storage(s_q, (int(qs[-1]), num_q_heads, head_dim), dtype)
+    w.query_start = qs
+    return w
+
+
+# the chunked-prefill batch: 16 sequences of the 70B-like GQA shape, each with a 512-token
+# chunk after a prior context uniform in [0, 3584] tokens
+PREFILL_RECIPE = ("chunked prefill bf16: 16 sequences, a 512-token chunk each after a prior "
+                  "context uniform in [0, 3584] tokens, 64 q heads over 8 KV heads, head_dim 128, "
+                  "block_size 16, shuffled pool sized to need + 10%, q/K/V ~ N(0,1)")
+
+
+def prefill_workload(*, seed: int = BASE_SEED + 6, num_seqs: int = 16, chunk: int = 512,
+                     max_prior: int = 3584) -> Workload:
+    """The chunked-prefill batch (seeded)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7])))
+    prior = rng.integers(0, max_prior, size=num_seqs, endpoint=True)
+    return make_prefill_workload("chunked-prefill-70b-gqa8-c512", seed=seed, dtype="bf16",
+                                 prior_lens=prior, chunk_lens=[chunk] * num_seqs, num_q_heads=64,
+                                 num_kv_heads=8, head_dim=128, block_size=16,
+                                 max_blocks_per_seq=(max_prior + chunk + 15) // 16)
 
 
 # ---------------------------------------------------------------------------------------
@@ -441,6 +487,9 @@ def to_torch(w: Workload, device):
         out["slot_mapping"] = torch.from_numpy(np.ascontiguousarray(w.slot_mapping)).to(device)
     if w.copy_pairs is not None:
         out["copy_pairs"] = torch.from_numpy(np.ascontiguousarray(w.copy_pairs)).to(device)
+    if w.chunk_q is not None:
+        out["chunk_q"] = elems(w.chunk_q)
+        out["query_start"] = torch.from_numpy(np.ascontiguousarray(w.query_start)).to(device)
     return out
 
 

@@ -560,3 +560,111 @@ def test_fp8_slot_write_quantises_like_torch(oracle_mod):
         np.testing.assert_array_equal(rows_k[sl], synth.e4m3_codes(kx[i], ks))
         np.testing.assert_array_equal(rows_v[sl], synth.e4m3_codes(vx[i], vs))
     assert (rows_k[[1, 2, 3]] == 0).all()
+
+
+# ----------------------------------------------------------------------------------------
+# chunked prefill ("Paged Attention: How vLLM Solves the KV Cache Memory Problem",
+# section "Continuous Batching and Chunked Prefill")
+# ----------------------------------------------------------------------------------------
+
+def _pf(dtype="bf16", prior=(0, 3, 16, 40), chunk=(5, 1, 17, 9), Hq=4, Hkv=2, D=64, bs=16,
+        shuffle=True, seed=21, scale=None, **kw):
+    return synth.make_prefill_workload("pin-pf", seed=seed, dtype=dtype, prior_lens=list(prior),
+                                       chunk_lens=list(chunk), num_q_heads=Hq, num_kv_heads=Hkv,
+                                       head_dim=D, block_size=bs, shuffle=shuffle, scale=scale,
+                                       **kw)
+
+
+def _run_pf(oracle_mod, w, **kw):
+    return oracle_mod.paged_prefill(w.chunk_q, w.k_cache, w.v_cache, w.block_tables,
+                                    w.context_lens, w.query_start, w.scale, w.dtype, **kw)
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,bs", [
+    ("f32", 4, 4, 64, 16), ("bf16", 8, 2, 128, 16), ("f16", 6, 3, 32, 32)])
+def test_prefill_matches_causal_sdpa_on_unpaged_sequence(oracle_mod, dtype, Hq, Hkv, D, bs):
+    """A chunk's rows equal causal attention over the prior context plus the chunk.
+
+    Reference: torch scaled_dot_product_attention in float64 on the sequence's
+    contiguous K/V rows (pool unshuffled) with an explicit mask: query i of an n-token
+    chunk may see key j iff j <= L - n + i.  Catches: an off-by-one in the causal limit,
+    queries placed at the start instead of the end of the context, a mask applied to
+    the prior context, wrong query rows per sequence, wrong head mapping.
+    """
+    w = _pf(dtype=dtype, prior=(0, 7, bs, 2 * bs + 3), chunk=(bs + 2, 1, 5, 2 * bs),
+            Hq=Hq, Hkv=Hkv, D=D, bs=bs, shuffle=False, scale=0.29)
+    out = _run_pf(oracle_mod, w)
+    G = Hq // Hkv
+    q = _f64(w, w.chunk_q)
+    for s in range(w.num_seqs):
+        k, v = _dense_rows(w, s)
+        L = int(w.context_lens[s])
+        a, b = int(w.query_start[s]), int(w.query_start[s + 1])
+        n = b - a
+        kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(G, dim=0)  # [Hq, L, D]
+        vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qt = torch.from_numpy(q[a:b]).permute(1, 0, 2)                          # [Hq, n, D]
+        mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]   # [n, L]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
+                                                               scale=w.scale)
+        np.testing.assert_allclose(out[a:b], ref.permute(1, 0, 2).numpy(), rtol=1e-12,
+                                   atol=1e-13)
+
+
+def test_prefill_row_equals_decode_of_truncated_context(oracle_mod):
+    """Row i of a chunk is a decode query over the first L - n + i + 1 tokens.
+
+    Reference: the decode oracle (its own pins above) run once per chunk row with the
+    context cut at the row's position, on the shuffled pool.  Catches: causal limit
+    errors, block-table walks that differ between the two paths, and results that
+    depend on tokens after the query.
+    """
+    w = _pf(prior=(0, 9, 33), chunk=(4, 12, 3), Hq=4, Hkv=2, D=64, bs=16, pool_slack=0.3)
+    out = _run_pf(oracle_mod, w)
+    for s in range(w.num_seqs):
+        L = int(w.context_lens[s])
+        a, b = int(w.query_start[s]), int(w.query_start[s + 1])
+        n = b - a
+        for i in range(n):
+            ref = oracle_mod.paged_decode(w.chunk_q[a + i][None], w.k_cache, w.v_cache,
+                                          w.block_tables[s:s + 1],
+                                          np.array([L - n + i + 1], np.int32), w.scale, w.dtype)
+            np.testing.assert_array_equal(out[a + i], ref[0])
+
+
+def test_prefill_of_one_token_chunks_is_decode(oracle_mod):
+    """With one query token per sequence the prefill oracle is the decode oracle.
+
+    Catches: treating the chunk as the first rather than the last n tokens, and any
+    special-casing of n = 1.
+    """
+    w = _pf(prior=(0, 15, 16, 63), chunk=(1, 1, 1, 1), Hq=8, Hkv=2, D=64, bs=16)
+    out = _run_pf(oracle_mod, w)
+    ref = oracle_mod.paged_decode(w.chunk_q, w.k_cache, w.v_cache, w.block_tables,
+                                  w.context_lens, w.scale, w.dtype)
+    np.testing.assert_array_equal(out, ref)
+
+
+def test_prefill_first_chunk_token_of_an_empty_context_returns_its_value(oracle_mod):
+    """The first token of a prompt's first chunk sees only itself: its output is V_0.
+
+    Catches: attending a token past the query, normalisation errors.
+    """
+    w = _pf(dtype="f32", prior=(0, 0), chunk=(3, 1), Hq=2, Hkv=1, D=32, bs=16)
+    out = _run_pf(oracle_mod, w)
+    for s in range(w.num_seqs):
+        a = int(w.query_start[s])
+        phys = int(w.block_tables[s, 0])
+        v0 = w.v_cache[phys, 0, 0].astype(np.float64)
+        for h in range(2):
+            np.testing.assert_array_equal(out[a, h], v0)
+
+
+def test_prefill_rejects_a_chunk_longer_than_its_context(oracle_mod):
+    w = _pf(prior=(0, 4), chunk=(3, 2), Hq=2, Hkv=1, D=32, bs=16)
+    qs = w.query_start.copy()
+    cl = w.context_lens.copy()
+    cl[1] = 1  # the second chunk has 2 rows but the context only 1 token
+    with pytest.raises(ValueError):
+        oracle_mod.paged_prefill(w.chunk_q, w.k_cache, w.v_cache, w.block_tables, cl, qs,
+                                 w.scale, w.dtype)

@@ -66,3 +66,26 @@ def test_config_shapes(cfg):
         assert len(set(w.copy_pairs[:, 1])) == 256
         assert (w.block_tables[:, 31] == w.copy_pairs[:, 1]).all()
         assert w.slot_mapping.shape[0] == int((w.context_lens - 1008).sum())
+
+
+def test_prefill_workload_packs_chunks_after_prior_context():
+    w = synth.make_prefill_workload("t", seed=3, dtype="bf16", prior_lens=[0, 20, 5],
+                                    chunk_lens=[4, 1, 30], num_q_heads=4, num_kv_heads=2,
+                                    head_dim=32, block_size=16)
+    assert w.query_start.tolist() == [0, 4, 5, 35]
+    assert w.context_lens.tolist() == [4, 21, 35]
+    assert w.chunk_q.shape == (35, 4, 32)
+    # the cache holds every token of prior + chunk: blocks for all of them are allocated
+    for s, L in enumerate(w.context_lens):
+        nb = -(-int(L) // 16)
+        assert (w.block_tables[s, :nb] >= 0).all()
+
+
+def test_prefill_batch_is_seeded_and_shaped():
+    a = synth.prefill_workload()
+    b = synth.prefill_workload()
+    assert np.array_equal(a.context_lens, b.context_lens)
+    assert np.array_equal(a.chunk_q, b.chunk_q)
+    assert a.num_seqs == 16 and a.chunk_q.shape == (16 * 512, 64, 128)
+    prior = a.context_lens - 512
+    assert prior.min() >= 0 and prior.max() <= 3584
