@@ -34,8 +34,10 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "paged decode attention KV-read GB/s (% of HBM peak) and queries/s per batch"
+PREFILL_METRIC = "paged chunked-prefill attention TFLOP/s (causal chunks over the paged cache)"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM bytes (read + write) per launch of the decode kernel, from one ncu capture per
 # workload and partition size, valid only for the kernel source whose hash is recorded
@@ -69,8 +71,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--kv-dtype", choices=["same", "fp8"], default="same",
                    help="cache element type: the batch's own (default) or fp8 E4M3 codes")
-    p.add_argument("--op", choices=["decode", "swap"], default="decode",
-                   help="decode (default): the decode step; swap: block swaps device <-> host")
+    p.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
+                   help="decode (default): the decode step; swap: block swaps device <-> host; "
+                        "prefill: chunked-prefill attention")
     p.add_argument("--swap-blocks", type=int, default=4096,
                    help="blocks per swap direction for --op swap")
     return p.parse_args(argv)
@@ -600,10 +603,237 @@ def run_swap(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------------------
+# chunked prefill
+# ------------------------------------------------------------------------------------------
+
+def prefill_flops(w: synth.Workload, seqs=None) -> int:
+    """Attention flops of the chunks: 4 * head_dim per (query row, head, attended key)."""
+    n = np.diff(w.query_start).astype(np.int64)
+    L = w.context_lens.astype(np.int64)
+    total = 0
+    for s in (range(w.num_seqs) if seqs is None else seqs):
+        ns, Ls = int(n[s]), int(L[s])
+        keys = (Ls - ns) * ns + ns * (ns + 1) // 2  # row i attends L - n + i + 1 keys
+        total += 4 * w.head_dim * w.num_q_heads * keys
+    return total
+
+
+def tensor_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def _oracle_prefill_seq(w, s):
+    """The oracle on sequence s alone (all its chunk rows)."""
+    import oracle
+
+    a, b = int(w.query_start[s]), int(w.query_start[s + 1])
+    return oracle.paged_prefill(w.chunk_q[a:b], w.k_cache, w.v_cache, w.block_tables[s:s + 1],
+                                w.context_lens[s:s + 1], np.array([0, b - a], np.int32), w.scale,
+                                w.dtype)
+
+
+def prefill_config(w) -> dict:
+    n = np.diff(w.query_start)
+    prior = w.context_lens - n
+    return {"workload": w.name, "recipe": synth.PREFILL_RECIPE, "sequences": w.num_seqs,
+            "chunk_tokens": int(n.max()), "prior_min_mean_max": [int(prior.min()),
+                                                                 float(prior.mean()),
+                                                                 int(prior.max())],
+            "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "flops_per_step": prefill_flops(w),
+            "l2": "not flushed: every step reads 134 MB of queries and ~150 MB of KV and writes "
+                  "134 MB, together above the 129 MiB L2"}
+
+
+def run_prefill(args) -> None:
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    w = synth.prefill_workload()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+
+        oracle.build()
+        for i in range(args.warmup):
+            _oracle_prefill_seq(w, i % w.num_seqs)
+        flops = 0
+        s0 = time.perf_counter()
+        for i in range(args.steps):
+            _oracle_prefill_seq(w, i % w.num_seqs)
+            flops += prefill_flops(w, [i % w.num_seqs])
+        el = time.perf_counter() - s0
+        value = flops / el / 1e12
+        line = {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
+                "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
+                "config": prefill_config(w),
+                "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                                 "cores": oracle.max_threads(), "kind": "oracle",
+                                 "sample": "one sequence's whole chunk per step, cycling through "
+                                           "the batch; fp64 C oracle, OpenMP"},
+                "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch.distributed as dist
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import paged_kv_cache_315_gb300 as pkv
+
+    pkv.load()
+    t = synth.to_torch(w, dev)
+    out = torch.empty_like(t["chunk_q"])
+    maxq = int(np.diff(w.query_start).max())
+    flops = prefill_flops(w)
+
+    def step(inp, ev=None):
+        if ev is not None:
+            ev[0].record()
+        pkv.paged_attn_prefill(out, inp["chunk_q"], t["k_cache"], t["v_cache"],
+                               inp["block_tables"], inp["context_lens"], inp["query_start"], maxq,
+                               w.scale)
+        if ev is not None:
+            ev[1].record()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step(t)
+    torch.cuda.synchronize()
+    if pkv.pkv_device_error() != 0:
+        raise RuntimeError("device error bits set during warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    t0.record()
+    for i in range(args.steps):
+        step(t, evs[i])
+    t1.record()
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if pkv.pkv_device_error() != 0:
+        raise RuntimeError("device error bits set during the timed steps")
+    elapsed_ms, kernel_ms = max_over_ranks([elapsed_ms, kernel_ms], world)
+
+    e2e = None
+    if not args.no_e2e:
+        names = ["chunk_q", "block_tables", "context_lens", "query_start"]
+        offsets, off = {}, 0
+        for n in names:
+            offsets[n] = off
+            off += -(-t[n].numel() * t[n].element_size() // 256) * 256
+        host_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
+        dev_buf = torch.empty(off, dtype=torch.uint8, device=dev)
+
+        def view(buf, n):
+            nb = t[n].numel() * t[n].element_size()
+            return buf[offsets[n]:offsets[n] + nb].view(t[n].dtype).view(t[n].shape)
+
+        for n in names:
+            view(host_buf, n).copy_(t[n].cpu())
+        dev_in = {n: view(dev_buf, n) for n in names}
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t[n].numel() * t[n].element_size() for n in names)
+        d2h = out_h.numel() * out_h.element_size()
+        stream = torch.cuda.current_stream()
+
+        def e2e_step():
+            dev_buf.copy_(host_buf, non_blocking=True)
+            step(dev_in)
+            out_h.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        barrier()
+        s0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        barrier()
+        e2e_s = time.perf_counter() - s0
+        (e2e_s,) = max_over_ranks([e2e_s], world)
+        e2e = {"value": round(flops * world * args.steps / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_s * 1e3 / args.steps, 4),
+               "path": "chunk queries and tables packed in one pinned host buffer -> one "
+                       "cudaMemcpyAsync -> C-ABI call -> output to pinned host, stream "
+                       "synchronised every step"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        done, nseq = 0, 0
+        s0 = time.perf_counter()
+        while True:
+            s = nseq % w.num_seqs
+            _oracle_prefill_seq(w, s)
+            done += prefill_flops(w, [s])
+            nseq += 1
+            el = time.perf_counter() - s0
+            if el >= args.cpu_seconds or nseq >= w.num_seqs:
+                break
+        cpu = {"value": round(done / el / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"{nseq} sequences' whole chunks in {el:.1f} s; fp64 C oracle, OpenMP "
+                         f"over (query row, head)"}
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = tensor_peak()
+    value = flops * world * args.steps / (elapsed_ms / 1e3) / 1e12
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
+        "config": prefill_config(w), "kernel_ms": round(kernel_ms, 5),
+        "roofline": {"kernel": "paged_attn_prefill (prefill_tc_kernel)", "bound": "tensor",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} bf16_tflops",
+                     "algorithmic_flops_per_launch": flops, "traffic": None},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.op == "swap":
         run_swap(args)
+        return
+    if args.op == "prefill":
+        run_prefill(args)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -165,6 +165,41 @@ int kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
                    int block_size, int num_blocks, pkv_dtype dtype, pkv_stream_t stream);
 
 /*
+ * paged_attn_prefill -- chunked-prefill attention: several query tokens per sequence
+ * over the paged cache, causal within the chunk.
+ *
+ * "Paged Attention: How vLLM Solves the KV Cache Memory Problem", section "Continuous
+ * Batching and Chunked Prefill": a long prompt is cut into chunks that are processed
+ * between decode steps.  Sequence s contributes the n_s = query_start[s+1] -
+ * query_start[s] query rows query_start[s] .. query_start[s+1]-1 of q.  Its cache already
+ * holds L_s = context_lens[s] tokens, the chunk's own keys and values last (written with
+ * kv_cache_write), so chunk token i sits at position L_s - n_s + i and attends positions
+ * 0 .. L_s - n_s + i:
+ *     out[t][h] = sum_{p <= L_s - n_s + i} softmax_p( scale * <q[t][h], K_p> ) * V_p,
+ * t = query_start[s] + i, K_p and V_p of KV head h / (num_q_heads / num_kv_heads) read
+ * through block_tables[s] as in paged_attn_decode.  A chunk of one token is a decode.
+ *
+ *   out, q       [num_q_tokens, num_q_heads, head_dim], `dtype` (PKV_BF16 or PKV_F16).
+ *   k_cache, v_cache, block_tables, context_lens, num_blocks: as in paged_attn_decode.
+ *   query_start  int32 [num_seqs + 1], device; query_start[0] = 0, non-decreasing,
+ *                query_start[num_seqs] = num_q_tokens.
+ *   max_query_len  an upper bound on every n_s (sizes the grid; host value).
+ * All pointers are caller-owned device memory; the call is asynchronous on `stream` and
+ * allocates nothing.  head_dim 64 or 128, block_size 16, 32 or 64.
+ * Device-side data errors set PKV_DERR_* bits (see pkv_device_error) and skip the unit:
+ * a chunk longer than its context or than max_query_len, a context longer than the table
+ * or rows outside [0, num_q_tokens) set PKV_DERR_CONTEXT and leave that sequence's rows
+ * unwritten; an out-of-range live block id sets PKV_DERR_BLOCK_ID and reads as zeros.
+ * Returns PKV_OK, PKV_EINVAL, PKV_EUNSUPPORTED or PKV_ECUDA.
+ */
+int paged_attn_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens,
+                       const int32_t* query_start, int num_seqs, int num_q_tokens,
+                       int max_query_len, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                       pkv_dtype dtype, pkv_stream_t stream);
+
+/*
  * paged_attn_decode_fp8 -- paged_attn_decode over caches of 8-bit E4M3 codes.
  *
  * "PagedAttention: how vLLM manages the KV cache", section "Keep the tensor formula

@@ -60,6 +60,9 @@ def load() -> ctypes.CDLL:
         lib.paged_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                                   i32, i32, f32, i32, i32, P]
         lib.paged_attn_decode_noalloc.restype = i32
+        lib.paged_attn_prefill.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                           i32, i32, i32, f32, i32, P]
+        lib.paged_attn_prefill.restype = i32
         lib.kv_cache_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
         lib.kv_cache_write.restype = i32
         lib.kv_copy_blocks.argtypes = [P, P, i32, sz, i32, P]
@@ -199,6 +202,38 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         bs, MB, NB, float(scale), _dtype(q), int(partition_size), ws_ptr, ws_bytes,
         _stream(stream))
     _check("paged_attn_decode", rc)
+    return out
+
+
+def paged_attn_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, block_tables: torch.Tensor,
+                       context_lens: torch.Tensor, query_start: torch.Tensor,
+                       max_query_len: int, scale: float, stream=None) -> torch.Tensor:
+    """Chunked-prefill attention over the paged cache; writes and returns ``out``.
+
+    ``q``/``out`` [T, Hq, D]: sequence s owns rows ``query_start[s] .. query_start[s+1]-1``
+    (int32 [B + 1] on the device), the last tokens of its ``context_lens[s]`` cached
+    tokens, each attending causally.  ``max_query_len`` bounds every chunk length.
+    """
+    T, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    B = context_lens.shape[0]
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (T, Hq, D):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if not (q.dtype == out.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q, out and the caches must share one element type")
+    if (block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32
+            or query_start.dtype != torch.int32):
+        raise TypeError("block_tables, context_lens and query_start must be int32")
+    if (block_tables.dim() != 2 or block_tables.shape[0] != B
+            or tuple(query_start.shape) != (B + 1,)):
+        raise ValueError("block_tables must be [B, MB] and query_start [B + 1]")
+    rc = load().paged_attn_prefill(
+        _cuda("out", out), _cuda("q", q), _cuda("k_cache", k_cache), _cuda("v_cache", v_cache),
+        _cuda("block_tables", block_tables), _cuda("context_lens", context_lens),
+        _cuda("query_start", query_start), B, T, int(max_query_len), Hq, Hkv, D, bs,
+        block_tables.shape[1], NB, float(scale), _dtype(q), _stream(stream))
+    _check("paged_attn_prefill", rc)
     return out
 
 

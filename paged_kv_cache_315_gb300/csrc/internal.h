@@ -55,6 +55,26 @@ bool decode_fp8_supported(pkv_dtype dtype, int head_dim, int block_size);
 
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start;
+  int num_seqs, num_q_tokens, max_query_len, num_q_heads, num_kv_heads, head_dim, block_size;
+  int max_blocks_per_seq, num_blocks;
+  float scale;
+  pkv_dtype dtype;
+  unsigned* err;
+};
+
+// Whether the chunked-prefill kernel serves this element type and shape.
+bool prefill_supported(pkv_dtype dtype, int head_dim, int block_size);
+
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
 int launch_kv_cache_write_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
                               const int64_t* slot_mapping, int num_tokens, int row_elems,
                               pkv_dtype src_dtype, long long num_rows, float k_scale,

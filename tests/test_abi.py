@@ -86,6 +86,18 @@ def test_argument_checks_return_before_any_cuda_call(lib):
     c.restype = ctypes.c_int
     assert c(null, null, ctypes.c_int(0), ctypes.c_size_t(64), 4, null) == 0
     assert c(null, null, ctypes.c_int(3), ctypes.c_size_t(64), 4, null) == -1
+    p = lib.paged_attn_prefill
+    p.restype = ctypes.c_int
+    pargs = lambda hq, hkv, d, bs, dt, ntok: (  # noqa: E731
+        null, null, null, null, null, null, null, ctypes.c_int(2), ctypes.c_int(ntok),
+        ctypes.c_int(8), ctypes.c_int(hq), ctypes.c_int(hkv), ctypes.c_int(d), ctypes.c_int(bs),
+        ctypes.c_int(8), ctypes.c_int(16), ctypes.c_float(0.1), ctypes.c_int(dt), null)
+    assert p(*pargs(6, 4, 128, 16, 1, 4)) == -1     # Hq % Hkv != 0
+    assert p(*pargs(8, 4, 128, 16, 0, 4)) == -4     # fp32 not served
+    assert p(*pargs(8, 4, 96, 16, 1, 4)) == -4      # head_dim not served
+    assert p(*pargs(8, 4, 128, 8, 1, 4)) == -4      # block_size not served
+    assert p(*pargs(8, 4, 128, 16, 1, 0)) == 0      # no query rows: nothing to do
+    assert p(*pargs(8, 4, 128, 16, 1, 4)) == -1     # null pointers
 
 
 def test_default_partition_size_follows_available_parallelism(lib):
@@ -107,3 +119,21 @@ def test_default_partition_size_follows_available_parallelism(lib):
     # the workspace query makes the same choice
     assert pkv.paged_attn_decode_workspace_size(4, 32, 8, 128, 16, 2048, 0) == \
         pkv.paged_attn_decode_workspace_size(4, 32, 8, 128, 16, 2048, 512)
+
+
+def test_binding_argument_lists_match_the_header():
+    """Every function the binding declares takes as many arguments as the header says."""
+    import paged_kv_cache_315_gb300._binding as bnd
+
+    lib = bnd.load()
+    text = "".join(open(os.path.join(HEADER_DIR, f)).read()
+                   for f in sorted(os.listdir(HEADER_DIR)) if f.endswith(".h"))
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    for name in _declared_functions():
+        m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+        assert m, name
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), len(params))
