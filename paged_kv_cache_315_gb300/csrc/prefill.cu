@@ -20,12 +20,18 @@
 // accumulation, an online softmax in base 2 with per-row causal limits, P rounded to the
 // operand type (row sums of the rounded P).  Keys past a row's limit are masked; value
 // rows past the context (stale slots of the last block) are zeroed in registers.
+//
+// Head size 128 with a power-of-two number of query heads per KV head takes the tcgen05
+// kernel further down (128-row tiles, accumulators in tensor memory); other shapes take
+// the mma.sync kernel.
 #include <algorithm>
 #include <climits>
 #include <mutex>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "umma.cuh"
 
 namespace pkv {
 namespace {
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(kPrefillThreads)
       if (lane == 0 && j >= P.stages)
         ok = mbar_wait_bounded(smem_addr(&empty[st]), ((j / P.stages) - 1) & 1) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok || flags[0]) {
+      if (!ok || __any_sync(0xffffffffu, flags[0] != 0)) {
         if (lane == 0 && !ok) {
           raise_error(P.err, PKV_DERR_TIMEOUT);
           flags[0] = 1;
@@ -204,8 +210,9 @@ __global__ void __launch_bounds__(kPrefillThreads)
       const int st = j % P.stages;
       const int t0 = j * kKeyTile;
       if (t0 <= wlim) {
-        if (flags[0]) break;
-        if (!mbar_wait_bounded(smem_addr(&full[st]), (j / P.stages) & 1)) {
+        // warp-uniform decisions: the fragment loads and MMAs below are warp-collective
+        if (__any_sync(0xffffffffu, flags[0] != 0)) break;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&full[st]), (j / P.stages) & 1))) {
           if (lane == 0) {
             raise_error(P.err, PKV_DERR_TIMEOUT);
             flags[0] = 1;
@@ -336,6 +343,385 @@ __global__ void __launch_bounds__(kPrefillThreads)
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// tcgen05 path: head_dim 128, a power-of-two number of query heads per KV head
+// ------------------------------------------------------------------------------------------
+//
+// One CTA per (sequence, KV head, 128 packed query rows).  Warps 0-3 run the softmax
+// (thread r owns row r, which is tensor-memory lane r), warp 4 produces (the Q tile with a
+// 3-D TMA box, then 64-token K and V tiles), warp 5 issues the MMAs from one thread.
+// Tensor memory (256 columns): two 64-column score buffers and the 128-column output.
+//   S_b = Q . K_j^T       (M 128, N 64, K 128; A and B K-major from shared memory)
+//   P_j                   (bf16, written over the first 32 columns of S_b)
+//   O  += P_j . V_j       (M 128, N 128, K 64; A from tensor memory, V MN-major)
+// The MMA thread issues QK(j) before PV(j-1), so the tensor cores score tile j while the
+// softmax warps turn tile j-1's scores into weights.  O stays in tensor memory for the
+// whole key range; the softmax reference max moves only when a row's scores exceed it by
+// more than kSlack, and only then are O's rows rescaled (after the previous PV is done).
+
+constexpr int kUThreads = 192;
+constexpr int kURows = 128;       // packed query rows per CTA
+constexpr int kUKeys = 64;        // key tokens per tile
+constexpr int kUStages = 2;       // K/V ring depth
+constexpr int kUTmemCols = 256;
+constexpr int kUTile = kUKeys * 128 * 2;   // bytes of a K (or V) tile, head_dim 128
+constexpr int kUQBytes = kURows * 128 * 2;
+constexpr int kUSmem = 1024 + kUQBytes + kUStages * 2 * kUTile + 256;
+
+template <typename T, int BS>
+__global__ void __launch_bounds__(kUThreads, 2)
+    prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap,
+                        const __grid_constant__ CUtensorMap qmap, const PrefillParams P) {
+  constexpr int D = 128;
+  constexpr int NBT = kUKeys / BS;
+  constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
+  constexpr uint32_t kIdQK = umma_idesc(kURows, kUKeys, kBf16, false);
+  constexpr uint32_t kIdPV = umma_idesc(kURows, D, kBf16, true);
+  extern __shared__ uint8_t smem_raw[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  long long bid = blockIdx.x;
+  const int g = static_cast<int>(bid % P.num_kv_heads);
+  bid /= P.num_kv_heads;
+  const int mt = P.m_tiles - 1 - static_cast<int>(bid % P.m_tiles);
+  const int s = static_cast<int>(bid / P.m_tiles);
+  const int q0 = P.query_start[s], q1 = P.query_start[s + 1];
+  const int n = q1 - q0;
+  const int L = P.context_lens[s];
+  const int G = P.group;
+  const int row0 = mt * kURows;
+  if (q0 < 0 || q1 > P.num_q_tokens || n < 0 || n > P.max_query_len || n > L ||
+      L > P.max_blocks_per_seq * P.block_size) {
+    if (tid == 0) raise_error(P.err, PKV_DERR_CONTEXT);
+    return;
+  }
+  if (row0 >= n * G) return;
+  const int rows = min(kURows, n * G - row0);
+  const int kmax = L - n + (row0 + rows - 1) / G;
+  const int ntiles = kmax / kUKeys + 1;
+  const int live_blocks = (L + BS - 1) / BS;
+
+  uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sq = base;
+  uint8_t* ring = base + kUQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kUStages * 2 * kUTile);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;                  // [kUStages]
+  uint64_t* kv_empty = kv_full + kUStages;       // [kUStages]
+  uint64_t* s_full = kv_empty + kUStages;        // [2]
+  uint64_t* p_full = s_full + 2;                 // [2]
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* drain = pv_done + 1;
+  uint32_t* tmem_base = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_base + 1);  // [0] abort, [1] issued
+
+  if (tid == 0) {
+    mbar_init(smem_addr(q_full), 1);
+    for (int i = 0; i < kUStages; ++i) {
+      mbar_init(smem_addr(&kv_full[i]), 1);
+      mbar_init(smem_addr(&kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&s_full[i]), 1);
+      mbar_init(smem_addr(&p_full[i]), 4);
+    }
+    mbar_init(smem_addr(pv_done), 1);
+    mbar_init(smem_addr(drain), 1);
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(tmem_base), kUTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tm = *tmem_base;
+  const uint32_t tm_o = tm + 2 * kUKeys;
+
+  auto fail = [&](void) {
+    raise_error(P.err, PKV_DERR_TIMEOUT);
+    flags[0] = 1;
+  };
+
+  if (warp == 4) {
+    // ---- producer -------------------------------------------------------------------------
+    const int32_t* bt = P.block_tables + static_cast<size_t>(s) * P.max_blocks_per_seq;
+    const int x0 = g * D;
+    if (lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&qmap);
+      const uint32_t bar = smem_addr(q_full);
+      mbar_arrive_expect_tx(bar, kUQBytes);
+      tma_load_3d(smem_addr(sq), &qmap, bar, 0, g * G, q0 + row0 / G);
+      tma_load_3d(smem_addr(sq) + kURows * 128, &qmap, bar, 64, g * G, q0 + row0 / G);
+    }
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % kUStages;
+      int y = P.num_blocks * BS;
+      if (lane < NBT) {
+        const int jb = j * NBT + lane;
+        if (jb < live_blocks) {
+          const int id = bt[jb];
+          if (id >= 0 && id < P.num_blocks)
+            y = id * BS;
+          else
+            raise_error(P.err, PKV_DERR_BLOCK_ID);
+        }
+      }
+      int ok = 1;
+      if (lane == 0 && j >= kUStages)
+        ok = mbar_wait_bounded(smem_addr(&kv_empty[st]), ((j / kUStages) - 1) & 1) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok || __any_sync(0xffffffffu, flags[0] != 0)) {
+        if (lane == 0 && !ok) fail();
+        break;
+      }
+      int ys[NBT];
+#pragma unroll
+      for (int k = 0; k < NBT; ++k) ys[k] = __shfl_sync(0xffffffffu, y, k);
+      if (lane == 0) {
+        const uint32_t bar = smem_addr(&kv_full[st]);
+        const uint32_t kdst = smem_addr(ring + st * 2 * kUTile);
+        const uint32_t vdst = kdst + kUTile;
+        mbar_arrive_expect_tx(bar, 2u * kUTile);
+#pragma unroll
+        for (int k = 0; k < NBT; ++k) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const uint32_t off = b * (kUKeys * 128) + k * (BS * 128);
+            tma_load_2d(kdst + off, &kmap, bar, x0 + b * 64, ys[k]);
+            tma_load_2d(vdst + off, &vmap, bar, x0 + b * 64, ys[k]);
+          }
+        }
+      }
+      issued = j + 1;
+    }
+    if (lane == 0) flags[1] = issued;
+  } else if (warp == 5) {
+    // ---- MMA issuer -----------------------------------------------------------------------
+    const uint32_t qb = smem_addr(sq);
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(smem_addr(q_full), 0) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && lane == 0) fail();
+    int issued_mma = 0;
+    auto pv = [&](int i) -> bool {  // O += P_i . V_i
+      const int st = i % kUStages, b = i & 1;
+      int okp = 1;
+      if (lane == 0) okp = mbar_wait_bounded(smem_addr(&p_full[b]), (i >> 1) & 1) ? 1 : 0;
+      okp = __shfl_sync(0xffffffffu, okp, 0);
+      if (!okp || __any_sync(0xffffffffu, flags[0] != 0)) {
+        if (lane == 0 && !okp) fail();
+        return false;
+      }
+      if (lane == 0) {
+        tc_fence_after_sync();
+        const uint32_t vb = smem_addr(ring + st * 2 * kUTile) + kUTile;
+#pragma unroll
+        for (int kt = 0; kt < kUKeys / 16; ++kt)
+          umma_ts(tm_o, tm + b * kUKeys + kt * 8, smem_desc_sw128(vb + kt * 2048, kUKeys * 128, 1024),
+                  kIdPV, (i > 0 || kt > 0) ? 1u : 0u);
+        umma_commit(smem_addr(&kv_empty[st]));
+        umma_commit(smem_addr(pv_done));
+      }
+      return true;
+    };
+    for (int j = 0; ok && j < ntiles; ++j) {
+      const int st = j % kUStages, b = j & 1;
+      // every lane observes the tile's arrival (the warp may zero part of it below)
+      const bool okk =
+          __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&kv_full[st]), (j / kUStages) & 1));
+      if (!okk || __any_sync(0xffffffffu, flags[0] != 0)) {
+        if (lane == 0 && !okk) fail();
+        ok = 0;
+        break;
+      }
+      // S_b still holds P_{j-2}: the P.V that reads it must be complete before QK(j)
+      // overwrites it
+      if (j >= 2) {
+        int okv = 1;
+        if (lane == 0) okv = mbar_wait_bounded(smem_addr(pv_done), (j - 2) & 1) ? 1 : 0;
+        okv = __shfl_sync(0xffffffffu, okv, 0);
+        if (!okv) {
+          if (lane == 0) fail();
+          ok = 0;
+          break;
+        }
+      }
+      const uint32_t kb = smem_addr(ring + st * 2 * kUTile);
+      if (lane == 0) {
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tm + b * kUKeys,
+                  smem_desc_sw128(qb + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024),
+                  smem_desc_sw128(kb + (kk >> 2) * (kUKeys * 128) + (kk & 3) * 32, 16, 1024),
+                  kIdQK, kk > 0 ? 1u : 0u);
+        umma_commit(smem_addr(&s_full[b]));
+      }
+      issued_mma = 1;
+      // value rows past the context (stale slots of the last block) become zeros before
+      // they meet zero weights in P.V
+      const int vrows = L - j * kUKeys;
+      if (vrows < kUKeys) {
+        uint8_t* vt = ring + st * 2 * kUTile + kUTile;
+        const int nz = (kUKeys - vrows) * 8;  // 16-byte chunks per box
+        for (int i = lane; i < 2 * nz; i += 32) {
+          const int bx = i / nz, rem = i - bx * nz;
+          *reinterpret_cast<uint4*>(vt + bx * (kUKeys * 128) + (vrows + rem / 8) * 128 +
+                                    (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (j > 0 && !pv(j - 1)) {
+        ok = 0;
+        break;
+      }
+    }
+    if (ok && ntiles > 0) pv(ntiles - 1);
+    // every MMA this thread issued is complete before tensor memory is released
+    if (lane == 0 && issued_mma) {
+      umma_commit(smem_addr(drain));
+      if (!mbar_wait_bounded(smem_addr(drain), 0)) fail();
+    }
+  } else {
+    // ---- softmax warps: thread r owns packed row r -------------------------------------
+    const int r = tid;
+    const int R = row0 + r;
+    const bool live = R < n * G;
+    const int Rc = live ? R : n * G - 1;
+    const int i = Rc / G;
+    const int head = g * G + (Rc - i * G);
+    const int lim = L - n + i;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    float m = -INFINITY, l = 0.f;
+    int done = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int b = j & 1;
+      // warp-uniform decisions: the tensor-memory accesses below are warp-collective
+      if (__any_sync(0xffffffffu, flags[0] != 0)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&s_full[b]), (j >> 1) & 1))) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after_sync();
+      uint32_t sraw[2][32];
+      tmem_ld32(tm + lane_off + b * kUKeys, sraw[0]);
+      tmem_ld32(tm + lane_off + b * kUKeys + 32, sraw[1]);
+      tmem_ld_wait();
+      const int t0 = j * kUKeys;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float v = __uint_as_float(sraw[h][c]) * P.scale_log2;
+          const float x = t0 + h * 32 + c <= lim ? v : -INFINITY;
+          sraw[h][c] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+      const bool up = mx > m + kSlack;
+      const float mn = up ? mx : m;
+      uint32_t pk[32];
+      float rs = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t w = Mma<T>::pack(exp2f(__uint_as_float(sraw[h][2 * c]) - mn),
+                                          exp2f(__uint_as_float(sraw[h][2 * c + 1]) - mn));
+          const float2 f = Mma<T>::unpack(w);
+          rs += f.x + f.y;
+          pk[h * 16 + c] = w;
+        }
+      const float alpha = exp2f(m - mn);  // 0 on the first tile (m = -inf), 1 if m stays
+      if (j > 0 && __any_sync(0xffffffffu, up)) {
+        // O's rows move to the new reference: the previous P.V must have landed
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(pv_done), (j - 1) & 1))) {
+          if (lane == 0) fail();
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int part = 0; part < D / 32; ++part) {
+          uint32_t ov[32];
+          tmem_ld32(tm_o + lane_off + part * 32, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st32(tm_o + lane_off + part * 32, ov);
+        }
+      }
+      l = l * alpha + rs;
+      m = mn;
+      tmem_st32(tm + lane_off + b * kUKeys, pk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&p_full[b]));
+      done = j + 1;
+    }
+    // the last P.V: waited on through `drain`, which the MMA thread commits after it (a
+    // parity wait on pv_done cannot tell PV(ntiles-1) from PV(ntiles-3))
+    if (done == ntiles && !__any_sync(0xffffffffu, flags[0] != 0)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(drain), 0))) {
+        if (lane == 0) fail();
+      } else {
+        tc_fence_after_sync();
+        const float inv = 1.f / l;
+        T* orow = static_cast<T*>(P.out) +
+                  (static_cast<size_t>(q0 + i) * P.num_q_heads + head) * D;
+#pragma unroll
+        for (int part = 0; part < D / 32; ++part) {
+          uint32_t ov[32];
+          tmem_ld32(tm_o + lane_off + part * 32, ov);
+          tmem_ld_wait();
+          if (live) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 8) {
+              uint4 v;
+              v.x = Mma<T>::pack(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+              v.y = Mma<T>::pack(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+              v.z = Mma<T>::pack(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+              v.w = Mma<T>::pack(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + part * 32 + c) = v;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // wait (bounded) for tile loads still in flight after an abort, then free tensor memory
+  if (tid == 4 * 32 && flags[0]) {
+    mbar_wait_bounded(smem_addr(q_full), 0);
+    const int issued = flags[1];
+    for (int j = max(0, issued - kUStages); j < issued; ++j)
+      mbar_wait_bounded(smem_addr(&kv_full[j % kUStages]), (j / kUStages) & 1);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 0) tmem_dealloc(tm, kUTmemCols);
+}
+
+using PrefillUmmaFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams);
+
+template <typename T>
+PrefillUmmaFn prefill_umma_for_type(int BS) {
+  if (BS == 16) return prefill_umma_kernel<T, 16>;
+  if (BS == 32) return prefill_umma_kernel<T, 32>;
+  if (BS == 64) return prefill_umma_kernel<T, 64>;
+  return nullptr;
+}
+
 using PrefillFn = void (*)(CUtensorMap, CUtensorMap, PrefillParams);
 
 template <typename T>
@@ -389,6 +775,31 @@ bool make_kv_map(CUtensorMap* map, const void* base, pkv_dtype dt, int Hkv, int 
          CUDA_SUCCESS;
 }
 
+// q [T, Hq, D] seen as 3-D (x = head_dim, y = query head, z = token): boxes of 64 columns
+// x G heads x 128 / G tokens, i.e. 128 packed rows of 128 bytes, 128-byte swizzle.
+bool make_q_map(CUtensorMap* map, const void* base, pkv_dtype dt, int T, int Hq, int D, int G) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  const CUtensorMapDataType t =
+      dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                              static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(Hq) * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, t, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// Whether the tcgen05 kernel serves this shape: head_dim 128 and a power-of-two number of
+// query heads per KV head, at most 128.
+bool umma_path(int head_dim, int group) {
+  return head_dim == 128 && group >= 1 && group <= 128 && (group & (group - 1)) == 0;
+}
+
 constexpr int kMaxPrefillSmem = 227 * 1024;
 
 }  // namespace
@@ -420,7 +831,9 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   P.block_size = BS;
   const long long packed = static_cast<long long>(a.max_query_len) * P.group;
   if (packed > INT_MAX / 2) return PKV_EUNSUPPORTED;
-  P.m_tiles = static_cast<int>((packed + kTileRows - 1) / kTileRows);
+  const bool umma = umma_path(D, P.group);
+  const int tile_rows = umma ? kURows : kTileRows;
+  P.m_tiles = static_cast<int>((packed + tile_rows - 1) / tile_rows);
   P.stage_bytes = 2 * kKeyTile * D * 2;
   P.stages = D == 128 ? 3 : 4;
   P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
@@ -434,6 +847,19 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (!make_kv_map(&kmap, a.k_cache, a.dtype, a.num_kv_heads, D, rows, BS) ||
       !make_kv_map(&vmap, a.v_cache, a.dtype, a.num_kv_heads, D, rows, BS))
     return PKV_ECUDA;
+  if (umma) {
+    CUtensorMap qmap;
+    if (!make_q_map(&qmap, a.q, a.dtype, a.num_q_tokens, a.num_q_heads, D, P.group))
+      return PKV_ECUDA;
+    PrefillUmmaFn ufn = a.dtype == PKV_BF16 ? prefill_umma_for_type<__nv_bfloat16>(BS)
+                                            : prefill_umma_for_type<__half>(BS);
+    if (!ufn) return PKV_EUNSUPPORTED;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void*>(ufn),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem) != cudaSuccess)
+      return PKV_ECUDA;
+    ufn<<<static_cast<unsigned>(grid), kUThreads, kUSmem, stream>>>(kmap, vmap, qmap, P);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
+  }
   PrefillFn fn = a.dtype == PKV_BF16 ? prefill_kernel_for_type<__nv_bfloat16>(D, BS)
                                      : prefill_kernel_for_type<__half>(D, BS);
   if (!fn) return PKV_EUNSUPPORTED;
