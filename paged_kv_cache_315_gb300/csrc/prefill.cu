@@ -348,8 +348,9 @@ __global__ void __launch_bounds__(kPrefillThreads)
 // ------------------------------------------------------------------------------------------
 //
 // One CTA per (sequence, KV head, 128 packed query rows).  Warps 0-3 run the softmax
-// (thread r owns row r, which is tensor-memory lane r), warp 4 produces (the Q tile with a
-// 3-D TMA box, then 64-token K and V tiles), warp 5 issues the MMAs from one thread.
+// (thread r owns row r, which is tensor-memory lane r), warp 4 loads the Q tile (one 3-D
+// TMA box per 64 columns) and the 64-token K tiles, warp 6 the V tiles, and warp 5 issues
+// the MMAs from one thread.
 // Tensor memory (256 columns): two 64-column score buffers and the 128-column output.
 //   S_b = Q . K_j^T       (M 128, N 64, K 128; A and B K-major from shared memory)
 //   P_j                   (bf16, written over the first 32 columns of S_b)
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(kPrefillThreads)
 // whole key range; the softmax reference max moves only when a row's scores exceed it by
 // more than kSlack, and only then are O's rows rescaled (after the previous PV is done).
 
-constexpr int kUThreads = 192;
+constexpr int kUThreads = 224;
 constexpr int kURows = 128;       // packed query rows per CTA
 constexpr int kUKeys = 64;        // key tokens per tile
 constexpr int kUStages = 2;       // K/V ring depth
@@ -407,20 +408,25 @@ __global__ void __launch_bounds__(kUThreads, 2)
   uint8_t* ring = base + kUQBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kUStages * 2 * kUTile);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;                  // [kUStages]
-  uint64_t* kv_empty = kv_full + kUStages;       // [kUStages]
-  uint64_t* s_full = kv_empty + kUStages;        // [2]
+  uint64_t* k_full = bars + 1;                   // [kUStages]
+  uint64_t* k_empty = k_full + kUStages;         // [kUStages]
+  uint64_t* v_full = k_empty + kUStages;         // [kUStages]
+  uint64_t* v_empty = v_full + kUStages;         // [kUStages]
+  uint64_t* s_full = v_empty + kUStages;         // [2]
   uint64_t* p_full = s_full + 2;                 // [2]
   uint64_t* pv_done = p_full + 2;
   uint64_t* drain = pv_done + 1;
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* flags = reinterpret_cast<volatile int*>(tmem_base + 1);  // [0] abort, [1] issued
+  // [0] abort, [1] K tiles issued, [2] V tiles issued
+  volatile int* flags = reinterpret_cast<volatile int*>(tmem_base + 1);
 
   if (tid == 0) {
     mbar_init(smem_addr(q_full), 1);
     for (int i = 0; i < kUStages; ++i) {
-      mbar_init(smem_addr(&kv_full[i]), 1);
-      mbar_init(smem_addr(&kv_empty[i]), 1);
+      mbar_init(smem_addr(&k_full[i]), 1);
+      mbar_init(smem_addr(&k_empty[i]), 1);
+      mbar_init(smem_addr(&v_full[i]), 1);
+      mbar_init(smem_addr(&v_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&s_full[i]), 1);
@@ -430,6 +436,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
     mbar_init(smem_addr(drain), 1);
     flags[0] = 0;
     flags[1] = 0;
+    flags[2] = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -447,18 +454,26 @@ __global__ void __launch_bounds__(kUThreads, 2)
     flags[0] = 1;
   };
 
-  if (warp == 4) {
-    // ---- producer -------------------------------------------------------------------------
+  if (warp == 4 || warp == 6) {
+    // ---- producers: warp 4 loads Q and the K tiles, warp 6 the V tiles ----------------
+    // A K slot frees when the QK that read it completes, a V slot when its PV completes,
+    // so each ring runs ahead by its own consumer.
+    const bool is_k = warp == 4;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    uint64_t* fullb = is_k ? k_full : v_full;
+    uint64_t* emptyb = is_k ? k_empty : v_empty;
+    const uint32_t tile_off = is_k ? 0u : static_cast<uint32_t>(kUTile);
     const int32_t* bt = P.block_tables + static_cast<size_t>(s) * P.max_blocks_per_seq;
     const int x0 = g * D;
     if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      tma_prefetch_desc(&qmap);
-      const uint32_t bar = smem_addr(q_full);
-      mbar_arrive_expect_tx(bar, kUQBytes);
-      tma_load_3d(smem_addr(sq), &qmap, bar, 0, g * G, q0 + row0 / G);
-      tma_load_3d(smem_addr(sq) + kURows * 128, &qmap, bar, 64, g * G, q0 + row0 / G);
+      tma_prefetch_desc(map);
+      if (is_k) {
+        tma_prefetch_desc(&qmap);
+        const uint32_t bar = smem_addr(q_full);
+        mbar_arrive_expect_tx(bar, kUQBytes);
+        tma_load_3d(smem_addr(sq), &qmap, bar, 0, g * G, q0 + row0 / G);
+        tma_load_3d(smem_addr(sq) + kURows * 128, &qmap, bar, 64, g * G, q0 + row0 / G);
+      }
     }
     int issued = 0;
     for (int j = 0; j < ntiles; ++j) {
@@ -470,13 +485,13 @@ __global__ void __launch_bounds__(kUThreads, 2)
           const int id = bt[jb];
           if (id >= 0 && id < P.num_blocks)
             y = id * BS;
-          else
+          else if (is_k)
             raise_error(P.err, PKV_DERR_BLOCK_ID);
         }
       }
       int ok = 1;
       if (lane == 0 && j >= kUStages)
-        ok = mbar_wait_bounded(smem_addr(&kv_empty[st]), ((j / kUStages) - 1) & 1) ? 1 : 0;
+        ok = mbar_wait_bounded(smem_addr(&emptyb[st]), ((j / kUStages) - 1) & 1) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok || __any_sync(0xffffffffu, flags[0] != 0)) {
         if (lane == 0 && !ok) fail();
@@ -486,23 +501,19 @@ __global__ void __launch_bounds__(kUThreads, 2)
 #pragma unroll
       for (int k = 0; k < NBT; ++k) ys[k] = __shfl_sync(0xffffffffu, y, k);
       if (lane == 0) {
-        const uint32_t bar = smem_addr(&kv_full[st]);
-        const uint32_t kdst = smem_addr(ring + st * 2 * kUTile);
-        const uint32_t vdst = kdst + kUTile;
-        mbar_arrive_expect_tx(bar, 2u * kUTile);
+        const uint32_t bar = smem_addr(&fullb[st]);
+        const uint32_t dst = smem_addr(ring + st * 2 * kUTile) + tile_off;
+        mbar_arrive_expect_tx(bar, kUTile);
 #pragma unroll
         for (int k = 0; k < NBT; ++k) {
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const uint32_t off = b * (kUKeys * 128) + k * (BS * 128);
-            tma_load_2d(kdst + off, &kmap, bar, x0 + b * 64, ys[k]);
-            tma_load_2d(vdst + off, &vmap, bar, x0 + b * 64, ys[k]);
-          }
+          for (int b = 0; b < 2; ++b)
+            tma_load_2d(dst + b * (kUKeys * 128) + k * (BS * 128), map, bar, x0 + b * 64, ys[k]);
         }
       }
       issued = j + 1;
     }
-    if (lane == 0) flags[1] = issued;
+    if (lane == 0) flags[is_k ? 1 : 2] = issued;
   } else if (warp == 5) {
     // ---- MMA issuer -----------------------------------------------------------------------
     const uint32_t qb = smem_addr(sq);
@@ -516,27 +527,44 @@ __global__ void __launch_bounds__(kUThreads, 2)
       int okp = 1;
       if (lane == 0) okp = mbar_wait_bounded(smem_addr(&p_full[b]), (i >> 1) & 1) ? 1 : 0;
       okp = __shfl_sync(0xffffffffu, okp, 0);
-      if (!okp || __any_sync(0xffffffffu, flags[0] != 0)) {
-        if (lane == 0 && !okp) fail();
+      // every lane observes the V tile's arrival (the warp may zero part of it)
+      const bool okv = okp && __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&v_full[st]),
+                                                                         (i / kUStages) & 1));
+      if (!okv || __any_sync(0xffffffffu, flags[0] != 0)) {
+        if (lane == 0 && !okv) fail();
         return false;
+      }
+      uint8_t* vt = ring + st * 2 * kUTile + kUTile;
+      // value rows past the context (stale slots of the last block) become zeros before
+      // they meet zero weights in P.V
+      const int vrows = L - i * kUKeys;
+      if (vrows < kUKeys) {
+        const int nz = (kUKeys - vrows) * 8;  // 16-byte chunks per box
+        for (int e = lane; e < 2 * nz; e += 32) {
+          const int bx = e / nz, rem = e - bx * nz;
+          *reinterpret_cast<uint4*>(vt + bx * (kUKeys * 128) + (vrows + rem / 8) * 128 +
+                                    (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
       }
       if (lane == 0) {
         tc_fence_after_sync();
-        const uint32_t vb = smem_addr(ring + st * 2 * kUTile) + kUTile;
+        const uint32_t vb = smem_addr(vt);
 #pragma unroll
         for (int kt = 0; kt < kUKeys / 16; ++kt)
           umma_ts(tm_o, tm + b * kUKeys + kt * 8, smem_desc_sw128(vb + kt * 2048, kUKeys * 128, 1024),
                   kIdPV, (i > 0 || kt > 0) ? 1u : 0u);
-        umma_commit(smem_addr(&kv_empty[st]));
+        umma_commit(smem_addr(&v_empty[st]));
         umma_commit(smem_addr(pv_done));
       }
       return true;
     };
     for (int j = 0; ok && j < ntiles; ++j) {
       const int st = j % kUStages, b = j & 1;
-      // every lane observes the tile's arrival (the warp may zero part of it below)
-      const bool okk =
-          __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&kv_full[st]), (j / kUStages) & 1));
+      int okk = 1;
+      if (lane == 0) okk = mbar_wait_bounded(smem_addr(&k_full[st]), (j / kUStages) & 1) ? 1 : 0;
+      okk = __shfl_sync(0xffffffffu, okk, 0);
       if (!okk || __any_sync(0xffffffffu, flags[0] != 0)) {
         if (lane == 0 && !okk) fail();
         ok = 0;
@@ -563,23 +591,10 @@ __global__ void __launch_bounds__(kUThreads, 2)
                   smem_desc_sw128(qb + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024),
                   smem_desc_sw128(kb + (kk >> 2) * (kUKeys * 128) + (kk & 3) * 32, 16, 1024),
                   kIdQK, kk > 0 ? 1u : 0u);
+        umma_commit(smem_addr(&k_empty[st]));
         umma_commit(smem_addr(&s_full[b]));
       }
       issued_mma = 1;
-      // value rows past the context (stale slots of the last block) become zeros before
-      // they meet zero weights in P.V
-      const int vrows = L - j * kUKeys;
-      if (vrows < kUKeys) {
-        uint8_t* vt = ring + st * 2 * kUTile + kUTile;
-        const int nz = (kUKeys - vrows) * 8;  // 16-byte chunks per box
-        for (int i = lane; i < 2 * nz; i += 32) {
-          const int bx = i / nz, rem = i - bx * nz;
-          *reinterpret_cast<uint4*>(vt + bx * (kUKeys * 128) + (vrows + rem / 8) * 128 +
-                                    (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
       if (j > 0 && !pv(j - 1)) {
         ok = 0;
         break;
@@ -700,11 +715,13 @@ __global__ void __launch_bounds__(kUThreads, 2)
   }
 
   // wait (bounded) for tile loads still in flight after an abort, then free tensor memory
-  if (tid == 4 * 32 && flags[0]) {
-    mbar_wait_bounded(smem_addr(q_full), 0);
-    const int issued = flags[1];
+  if ((tid == 4 * 32 || tid == 6 * 32) && flags[0]) {
+    const bool is_k = tid == 4 * 32;
+    if (is_k) mbar_wait_bounded(smem_addr(q_full), 0);
+    uint64_t* fullb = is_k ? k_full : v_full;
+    const int issued = flags[is_k ? 1 : 2];
     for (int j = max(0, issued - kUStages); j < issued; ++j)
-      mbar_wait_bounded(smem_addr(&kv_full[j % kUStages]), (j / kUStages) & 1);
+      mbar_wait_bounded(smem_addr(&fullb[j % kUStages]), (j / kUStages) & 1);
   }
   tc_fence_before_sync();
   __syncthreads();
