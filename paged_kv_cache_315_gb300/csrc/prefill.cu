@@ -61,6 +61,13 @@ __device__ __forceinline__ uint32_t swz(int r, int d) {
                                ((((d & 63) >> 3) ^ (r & 7)) << 4));
 }
 
+// 2^x by the hardware approximation (MUFU.EX2; results below the normal range flush to 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t keep_lo_hi(uint32_t w, bool lo, bool hi) {
   return w & ((lo ? 0x0000ffffu : 0u) | (hi ? 0xffff0000u : 0u));
 }
@@ -631,30 +638,40 @@ __global__ void __launch_bounds__(kUThreads, 2)
       tmem_ld32(tm + lane_off + b * kUKeys, sraw[0]);
       tmem_ld32(tm + lane_off + b * kUKeys + 32, sraw[1]);
       tmem_ld_wait();
-      const int t0 = j * kUKeys;
-      float mx = -INFINITY;
+      // scores past the row's causal limit are masked (only tiles that cross it); the
+      // maximum is taken on the raw scores and the scale folds into one FFMA per score
+      const int rl = lim - j * kUKeys;  // last allowed key index within the tile
+      float mxr = -INFINITY;
+      if (rl >= kUKeys - 1) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float v = __uint_as_float(sraw[h][c]) * P.scale_log2;
-          const float x = t0 + h * 32 + c <= lim ? v : -INFINITY;
-          sraw[h][c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
+          for (int c = 0; c < 32; ++c) mxr = fmaxf(mxr, __uint_as_float(sraw[h][c]));
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float v = h * 32 + c <= rl ? __uint_as_float(sraw[h][c]) : -INFINITY;
+            sraw[h][c] = __float_as_uint(v);
+            mxr = fmaxf(mxr, v);
+          }
+      }
+      const float sl2 = P.scale_log2;  // > 0 (the launcher sends other scales elsewhere)
+      const float mx = mxr * sl2;
       const bool up = mx > m + kSlack;
       const float mn = up ? mx : m;
+      const float nmn = -mn;
       uint32_t pk[32];
       float rs = 0.f;
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const uint32_t w = Mma<T>::pack(exp2f(__uint_as_float(sraw[h][2 * c]) - mn),
-                                          exp2f(__uint_as_float(sraw[h][2 * c + 1]) - mn));
-          const float2 f = Mma<T>::unpack(w);
-          rs += f.x + f.y;
-          pk[h * 16 + c] = w;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sraw[h][2 * c]), sl2, nmn));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sraw[h][2 * c + 1]), sl2, nmn));
+          rs += p0 + p1;
+          pk[h * 16 + c] = Mma<T>::pack(p0, p1);
         }
       const float alpha = exp2f(m - mn);  // 0 on the first tile (m = -inf), 1 if m stays
       if (j > 0 && __any_sync(0xffffffffu, up)) {
@@ -848,7 +865,7 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   P.block_size = BS;
   const long long packed = static_cast<long long>(a.max_query_len) * P.group;
   if (packed > INT_MAX / 2) return PKV_EUNSUPPORTED;
-  const bool umma = umma_path(D, P.group);
+  const bool umma = umma_path(D, P.group) && a.scale > 0.f;
   const int tile_rows = umma ? kURows : kTileRows;
   P.m_tiles = static_cast<int>((packed + tile_rows - 1) / tile_rows);
   P.stage_bytes = 2 * kKeyTile * D * 2;
