@@ -607,6 +607,19 @@ def run_swap(args) -> None:
 # chunked prefill
 # ------------------------------------------------------------------------------------------
 
+# DRAM bytes (read + write) per launch of the chunked-prefill kernel on the chunked-prefill
+# batch, from one ncu capture, valid only for the kernel source whose hash is recorded.
+PREFILL_TRAFFIC = {"bytes": 278724864 + 106318080, "prefill_cu_sha": "9bd66ea7247fc2e3"}
+
+
+def prefill_traffic() -> float | None:
+    import hashlib
+
+    src = os.path.join(ROOT, "paged_kv_cache_315_gb300", "csrc", "prefill.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return float(PREFILL_TRAFFIC["bytes"]) if PREFILL_TRAFFIC["prefill_cu_sha"] == digest else None
+
+
 def prefill_flops(w: synth.Workload, seqs=None) -> int:
     """Attention flops of the chunks: 4 * head_dim per (query row, head, attended key)."""
     n = np.diff(w.query_start).astype(np.int64)
@@ -816,10 +829,11 @@ def run_prefill(args) -> None:
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
         "config": prefill_config(w), "kernel_ms": round(kernel_ms, 5),
-        "roofline": {"kernel": "paged_attn_prefill (prefill_tc_kernel)", "bound": "tensor",
+        "roofline": {"kernel": "paged_attn_prefill (prefill_umma_kernel)", "bound": "tensor",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} bf16_tflops",
-                     "algorithmic_flops_per_launch": flops, "traffic": None},
+                     "algorithmic_flops_per_launch": flops, "traffic": prefill_traffic(),
+                     "traffic_unit": "DRAM bytes per launch"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
     }
     print(json.dumps(line), flush=True)
