@@ -76,6 +76,12 @@ def parse_args(argv=None):
                         "prefill: chunked-prefill attention")
     p.add_argument("--swap-blocks", type=int, default=4096,
                    help="blocks per swap direction for --op swap")
+    p.add_argument("--shared-prefix", action="store_true",
+                   help="decode the shared-prefix batches (--config 4, --grouped-prefix) as a "
+                        "cascade over their shared prefixes (paged_attn_decode_shared_prefix)")
+    p.add_argument("--grouped-prefix", action="store_true",
+                   help="decode batch: 64 groups x 8 sequences sharing 4096-token prompts "
+                        "(parallel sampling) instead of --config")
     return p.parse_args(argv)
 
 
@@ -125,7 +131,8 @@ def algorithmic_bytes(w: synth.Workload, fp8: bool = False) -> dict:
 
 def describe(w: synth.Workload, cfg: int, part: int) -> dict:
     pool = 2 * w.k_cache.nbytes
-    d = {"workload": w.name, "recipe": synth.CONFIGS[cfg], "batch": w.num_seqs,
+    recipe = synth.GROUPED_PREFIX_RECIPE if "group_start" in w.info else synth.CONFIGS[cfg]
+    d = {"workload": w.name, "recipe": recipe, "batch": w.num_seqs,
          "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
          "block_size": w.block_size,
          "context_tokens": int(w.context_lens.sum()),
@@ -134,7 +141,11 @@ def describe(w: synth.Workload, cfg: int, part: int) -> dict:
          "pool_bytes": pool,
          "l2": f"not flushed: every step reads {w.kv_bytes() / 1e9:.2f} GB of KV, "
                f"{w.kv_bytes() / L2_BYTES:.0f}x the {L2_BYTES >> 20} MiB L2"}
-    if cfg == 4:
+    if "group_start" in w.info:
+        d["l2"] = ("not flushed: 64 prompts of 16 MB (1 GB, 8x the L2) are each read by their "
+                   "8 sequences in every step; value counts logical bytes")
+        d["unique_kv_bytes"] = unique_kv_bytes(w)
+    elif cfg == 4:
         d["l2"] = ("not flushed: the 32 shared prefix blocks (4 MB) are read by all 256 "
                    "sequences in every step and stay in L2; value counts logical bytes")
         d["unique_kv_bytes"] = unique_kv_bytes(w)
@@ -267,7 +278,11 @@ def run_ours(args) -> None:
 
     pkv.load()
     cfg = args.config
-    w = bench_workload(cfg)
+    if args.grouped_prefix:
+        w = synth.grouped_prefix_workload()
+        synth.add_new_tokens(w, seed=synth.BASE_SEED + 107)
+    else:
+        w = bench_workload(cfg)
     part = w.partition_size if args.partition < 0 else args.partition
     t = synth.to_torch(w, dev)
     fp8 = args.kv_dtype == "fp8"
@@ -297,6 +312,21 @@ def run_ours(args) -> None:
         B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.max_blocks_per_seq, part))
     has_pairs = "copy_pairs" in t
 
+    cascade = bool(args.shared_prefix)
+    if cascade:
+        if "shared_prefix_tokens" not in w.info or fp8:
+            raise SystemExit("--shared-prefix applies to the shared-prefix batches (--config 4, "
+                             "--grouped-prefix) with the bf16 cache")
+        gs = w.info.get("group_start", np.array([0, B], np.int32))
+        pls = w.info.get("prefix_lens", np.array([w.info["shared_prefix_tokens"]], np.int32))
+        t["group_start"] = torch.from_numpy(np.ascontiguousarray(gs, np.int32)).to(dev)
+        t["prefix_lens"] = torch.from_numpy(np.ascontiguousarray(pls, np.int32)).to(dev)
+        sp_max_group = int(np.diff(gs).max())
+        sp_max_prefix = int(pls.max())
+        sp_ws = pkv.workspace_for(dev, pkv.paged_attn_decode_shared_prefix_workspace_size(
+            B, len(pls), w.num_q_heads, w.num_kv_heads, w.block_size, w.max_blocks_per_seq,
+            sp_max_group, sp_max_prefix))
+
     def step(inp, ev=None):
         if has_pairs:
             pkv.kv_copy_blocks(t["k_cache"], inp["copy_pairs"])
@@ -309,7 +339,12 @@ def run_ours(args) -> None:
                                inp["slot_mapping"])
         if ev is not None:
             ev[0].record()
-        if fp8:
+        if cascade:
+            pkv.paged_attn_decode_shared_prefix(
+                out, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
+                inp["context_lens"], t["group_start"], t["prefix_lens"], sp_max_group,
+                sp_max_prefix, w.scale, workspace=sp_ws)
+        elif fp8:
             pkv.paged_attn_decode_fp8(out, inp["q"], t["k_cache"], t["v_cache"],
                                       inp["block_tables"], inp["context_lens"], w.scale, ks, vs,
                                       partition_size=part, workspace=ws)
@@ -324,6 +359,8 @@ def run_ours(args) -> None:
     # (the batches here stay far below the prep kernel's 65536-item limit)
     split = ws is not None and ws.numel() > 0
     launches_per_step = (2 if has_pairs else 0) + 1 + 1 + (2 if split else 0)
+    if cascade:  # prep, prefix pass, suffix ordering + decode, merge
+        launches_per_step = (2 if has_pairs else 0) + 1 + 5
     assert pkv.pkv_device_error() == 0
     for _ in range(args.warmup):
         step(t)
@@ -427,20 +464,23 @@ def run_ours(args) -> None:
         "vs_baseline": None,
         "dtype": w.dtype if not fp8 else f"{w.dtype} (E4M3 KV cache)",
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
-        "config": describe(w, cfg, part),
+        "config": dict(describe(w, cfg, part),
+                       **({"decode": "shared-prefix cascade"} if cascade else {})),
         "hbm_frac": round(value / peak, 4),
         "queries_per_s": round(B * world / (ms / 1e3), 1),
         "query_heads_per_s": round(B * w.num_q_heads * world / (ms / 1e3), 1),
         "decode_ms": round(decode_ms, 5),
         "partition_tokens": part,
         "kv_dtype": "e4m3" if fp8 else w.dtype,
-        "roofline": {"kernel": ("paged_attn_decode_fp8 (decode_fp8_kernel" if fp8
-                                else "paged_attn_decode (decode_tc_kernel")
-                     + (" + prep + merge grids)" if split else ")"), "bound": "hbm",
+        "roofline": {"kernel": ("paged_attn_decode_shared_prefix (prep, prefix and suffix "
+                                "passes of prefill_umma_kernel, merge)" if cascade else
+                                ("paged_attn_decode_fp8 (decode_fp8_kernel" if fp8
+                                 else "paged_attn_decode (decode_tc_kernel")
+                                + (" + prep + merge grids)" if split else ")")), "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": ab,
-                     "traffic": traffic_for(w.name, part, fp8)},
+                     "traffic": None if cascade else traffic_for(w.name, part, fp8)},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

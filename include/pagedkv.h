@@ -200,6 +200,51 @@ int paged_attn_prefill(void* out, const void* q, const void* k_cache, const void
                        pkv_dtype dtype, pkv_stream_t stream);
 
 /*
+ * paged_attn_decode_shared_prefix -- paged_attn_decode for sequences that share a
+ * physical prefix, reading each shared block once per group instead of once per sequence.
+ *
+ * "PagedAttention: how vLLM manages the KV cache", section "Copy-on-write makes shared
+ * prefixes practical": sequences forked from one prompt map the same physical blocks for
+ * their common prefix.  The result is paged_attn_decode's:
+ *     out[s][h] = sum_{p < L_s} softmax_p( scale * <q[s][h], K_p> ) * V_p,
+ * computed as a cascade: a prefix pass in which all queries of a group meet each prefix
+ * block once (tensor cores), a suffix pass (the decode kernel) over each sequence's own
+ * tokens, and a log-sum-exp merge of their partial results.
+ *
+ *   out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, ..., dtype:
+ *                as in paged_attn_decode (dtype PKV_BF16 or PKV_F16, head_dim 128,
+ *                block_size 16, 32 or 64, a power-of-two number of query heads per KV
+ *                head, scale > 0).
+ *   group_start  int32 [num_groups + 1], device: group g is the run of sequences
+ *                group_start[g] .. group_start[g+1]-1 (non-decreasing, within
+ *                [0, num_seqs]); sequences outside every run have no shared prefix.
+ *   prefix_lens  int32 [num_groups], device: the group's shared prefix in tokens, a
+ *                multiple of block_size, at most every member's context length.  The
+ *                members' block tables must hold the same physical ids for those blocks
+ *                (the first member's are read).
+ *   max_group_size, max_prefix_tokens  host upper bounds of the group sizes and prefix
+ *                lengths (they size the grids and the workspace).
+ *   workspace    device scratch of paged_attn_decode_shared_prefix_workspace_size() bytes
+ *                (16-byte aligned); it needs no initialisation.
+ * A group that breaks these rules sets PKV_DERR_CONTEXT; its members are then attended
+ * without the prefix pass (still correctly, if their tables are valid).
+ * Returns PKV_OK, PKV_EINVAL, PKV_ENOMEM, PKV_EUNSUPPORTED or PKV_ECUDA.
+ */
+size_t paged_attn_decode_shared_prefix_workspace_size(int num_seqs, int num_groups,
+                                                      int num_q_heads, int num_kv_heads,
+                                                      int block_size, int max_blocks_per_seq,
+                                                      int max_group_size, int max_prefix_tokens);
+int paged_attn_decode_shared_prefix(void* out, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* block_tables,
+                                    const int32_t* context_lens, const int32_t* group_start,
+                                    const int32_t* prefix_lens, int num_seqs, int num_groups,
+                                    int max_group_size, int max_prefix_tokens, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int num_blocks, float scale,
+                                    pkv_dtype dtype, void* workspace, size_t workspace_bytes,
+                                    pkv_stream_t stream);
+
+/*
  * paged_attn_decode_fp8 -- paged_attn_decode over caches of 8-bit E4M3 codes.
  *
  * "PagedAttention: how vLLM manages the KV cache", section "Keep the tensor formula

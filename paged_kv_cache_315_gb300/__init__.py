@@ -33,6 +33,8 @@ from ._binding import (  # noqa: F401
     paged_attn_decode_noalloc,
     paged_attn_decode_partition_tokens,
     paged_attn_prefill,
+    paged_attn_decode_shared_prefix,
+    paged_attn_decode_shared_prefix_workspace_size,
     paged_attn_decode_workspace_size,
     pkv_device_error,
     pkv_selftest_bounded_wait,

@@ -63,6 +63,13 @@ def load() -> ctypes.CDLL:
         lib.paged_attn_prefill.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                            i32, i32, i32, f32, i32, P]
         lib.paged_attn_prefill.restype = i32
+        lib.paged_attn_decode_shared_prefix_workspace_size.argtypes = [i32, i32, i32, i32, i32,
+                                                                       i32, i32, i32]
+        lib.paged_attn_decode_shared_prefix_workspace_size.restype = sz
+        lib.paged_attn_decode_shared_prefix.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32,
+                                                        i32, i32, i32, i32, i32, i32, i32, f32,
+                                                        i32, P, sz, P]
+        lib.paged_attn_decode_shared_prefix.restype = i32
         lib.kv_cache_write.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]
         lib.kv_cache_write.restype = i32
         lib.kv_copy_blocks.argtypes = [P, P, i32, sz, i32, P]
@@ -234,6 +241,58 @@ def paged_attn_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor
         _cuda("query_start", query_start), B, T, int(max_query_len), Hq, Hkv, D, bs,
         block_tables.shape[1], NB, float(scale), _dtype(q), _stream(stream))
     _check("paged_attn_prefill", rc)
+    return out
+
+
+def paged_attn_decode_shared_prefix_workspace_size(num_seqs: int, num_groups: int,
+                                                   num_q_heads: int, num_kv_heads: int,
+                                                   block_size: int, max_blocks_per_seq: int,
+                                                   max_group_size: int,
+                                                   max_prefix_tokens: int) -> int:
+    return int(load().paged_attn_decode_shared_prefix_workspace_size(
+        num_seqs, num_groups, num_q_heads, num_kv_heads, block_size, max_blocks_per_seq,
+        max_group_size, max_prefix_tokens))
+
+
+def paged_attn_decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                    v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                    context_lens: torch.Tensor, group_start: torch.Tensor,
+                                    prefix_lens: torch.Tensor, max_group_size: int,
+                                    max_prefix_tokens: int, scale: float,
+                                    workspace: torch.Tensor | None = None,
+                                    stream=None) -> torch.Tensor:
+    """Decode attention for groups of sequences sharing a physical prefix (a cascade).
+
+    Group g is the run of sequences ``group_start[g] .. group_start[g+1]-1`` (int32
+    [G + 1]); its first ``prefix_lens[g]`` tokens (int32 [G], whole blocks) are shared.
+    Same result as ``paged_attn_decode``.
+    """
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    G = prefix_lens.shape[0]
+    if D2 != D or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != (B, Hq, D):
+        raise ValueError("shape mismatch between q, out and the caches")
+    if not (q.dtype == out.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q, out and the caches must share one element type")
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                    ("group_start", group_start), ("prefix_lens", prefix_lens)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    if tuple(group_start.shape) != (G + 1,):
+        raise ValueError("group_start must be [num_groups + 1]")
+    need = paged_attn_decode_shared_prefix_workspace_size(B, G, Hq, Hkv, bs, block_tables.shape[1],
+                                                          max_group_size, max_prefix_tokens)
+    if workspace is None:
+        workspace = workspace_for(q.device, need)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().paged_attn_decode_shared_prefix(
+        _cuda("out", out), _cuda("q", q), _cuda("k_cache", k_cache), _cuda("v_cache", v_cache),
+        _cuda("block_tables", block_tables), _cuda("context_lens", context_lens),
+        _cuda("group_start", group_start), _cuda("prefix_lens", prefix_lens), B, G,
+        int(max_group_size), int(max_prefix_tokens), Hq, Hkv, D, bs, block_tables.shape[1], NB,
+        float(scale), _dtype(q), _cuda("workspace", workspace) if workspace is not None else None,
+        ws_bytes, _stream(stream))
+    _check("paged_attn_decode_shared_prefix", rc)
     return out
 
 

@@ -223,6 +223,74 @@ int paged_attn_prefill(void* out, const void* q, const void* k_cache, const void
   return launch_prefill(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t paged_attn_decode_shared_prefix_workspace_size(int num_seqs, int num_groups,
+                                                      int num_q_heads, int num_kv_heads,
+                                                      int block_size, int max_blocks_per_seq,
+                                                      int max_group_size, int max_prefix_tokens) {
+  if (num_seqs <= 0 || num_groups < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0 || block_size <= 0 || max_blocks_per_seq <= 0 ||
+      max_group_size < 0 || max_prefix_tokens < 0)
+    return 0;
+  return shared_prefix_workspace_size(num_seqs, num_groups, num_q_heads, num_kv_heads,
+                                      block_size, max_blocks_per_seq, max_group_size,
+                                      max_prefix_tokens);
+}
+
+int paged_attn_decode_shared_prefix(void* out, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* block_tables,
+                                    const int32_t* context_lens, const int32_t* group_start,
+                                    const int32_t* prefix_lens, int num_seqs, int num_groups,
+                                    int max_group_size, int max_prefix_tokens, int num_q_heads,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int num_blocks, float scale,
+                                    pkv_dtype dtype, void* workspace, size_t workspace_bytes,
+                                    pkv_stream_t stream) {
+  if (num_seqs < 0 || num_groups < 0 || max_group_size < 0 || max_prefix_tokens < 0 ||
+      num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0 || num_blocks <= 0 || !valid_dtype(dtype))
+    return PKV_EINVAL;
+  if (num_q_heads % num_kv_heads != 0) return PKV_EINVAL;
+  if (static_cast<long long>(num_blocks) * block_size >= INT_MAX) return PKV_EINVAL;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size >= INT_MAX) return PKV_EINVAL;
+  if (!prefill_umma_supported(dtype, head_dim, block_size, num_q_heads / num_kv_heads, scale))
+    return PKV_EUNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens ||
+      (num_groups > 0 && (!group_start || !prefix_lens)))
+    return PKV_EINVAL;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 4) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(group_start, 4) ||
+      !aligned(prefix_lens, 4) || !aligned(workspace, 16))
+    return PKV_EINVAL;
+  unsigned* err = error_word();
+  if (!err) return PKV_ECUDA;
+  SharedPrefixArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.group_start = group_start;
+  a.prefix_lens = prefix_lens;
+  a.num_seqs = num_seqs;
+  a.num_groups = num_groups;
+  a.max_group_size = max_group_size;
+  a.max_prefix_tokens = max_prefix_tokens;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err = err;
+  return launch_shared_prefix(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
                    const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
                    int block_size, int num_blocks, pkv_dtype dtype, pkv_stream_t stream) {

@@ -70,6 +70,7 @@ struct Params {
   int max_groups;   // CTAs per (sequence, KV head, head chunk) = ceil(max_parts / ppc)
   int merge_off;    // byte offset of the merge buffer from the ring (0: the ring itself)
   const int32_t* order;  // CTA work order over (sequence, partition group) items, or null
+  int force_partials;    // every context leaves (m, l, o) partials, none writes `out`
   float scale_log2;
   float out_scale;  // multiplies every output (the V scale of fp8 caches, else 1)
 };
@@ -236,7 +237,7 @@ __device__ void finish(const Params& P, const Work& w, int D, int HC, const floa
                        const float* ml_s) {
   const int tid = threadIdx.x;
   const int n = w.hc * D;
-  const bool split = w.np > 1;
+  const bool split = w.np > 1 || P.force_partials;
   T* out = static_cast<T*>(P.out);
   for (int i = tid; i < n; i += kThreads) {
     const int r = i / D, d = i - r * D;
@@ -1075,11 +1076,11 @@ int resolve_partition_tokens(int partition_size, int block_size, int num_seqs, i
 }
 
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int block_size,
-                                 int max_blocks_per_seq, int partition_tokens) {
+                                 int max_blocks_per_seq, int partition_tokens, bool partials) {
   WorkspaceLayout w{};
   const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
   w.max_parts = static_cast<int>(std::max(1LL, (max_ctx + partition_tokens - 1) / partition_tokens));
-  if (w.max_parts <= 1) return w;
+  if (w.max_parts <= 1 && !partials) return w;
   const size_t units = static_cast<size_t>(num_seqs) * num_q_heads * w.max_parts;
   w.o_offset = 0;
   w.ml_offset = align_up(units * head_dim * sizeof(float), 256);
@@ -1114,7 +1115,8 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const bool tc = a.kv_fp8 || decode_uses_tensor_cores(a.dtype, a.head_dim, a.block_size);
   const int D = a.head_dim, BS = a.block_size;
   const WorkspaceLayout wl = workspace_layout(a.num_seqs, a.num_q_heads, D, BS,
-                                              a.max_blocks_per_seq, a.partition_tokens);
+                                              a.max_blocks_per_seq, a.partition_tokens,
+                                              a.partials_out);
   if (wl.max_parts > kMaxParts) return PKV_EUNSUPPORTED;
   if (wl.total > 0 && (a.workspace == nullptr || a.workspace_bytes < wl.total)) return PKV_ENOMEM;
 
@@ -1135,6 +1137,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   P.block_size = BS;
   P.partition_blocks = a.partition_tokens / BS;
   P.max_parts = wl.max_parts;
+  P.force_partials = a.partials_out ? 1 : 0;
   if (wl.total > 0) {
     char* ws = static_cast<char*>(a.workspace);
     P.ws_o = reinterpret_cast<float*>(ws + wl.o_offset);
@@ -1184,8 +1187,9 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
                          : kernel_for(a.dtype, D, BS, tc);
   if (!fn) return PKV_EUNSUPPORTED;
   const bool split = wl.total > 0;
-  MergeFn merge = split ? merge_kernel_for(a.dtype, D) : nullptr;
-  if (split && !merge) return PKV_EUNSUPPORTED;
+  // with partials_out the caller merges the partials itself
+  MergeFn merge = split && !a.partials_out ? merge_kernel_for(a.dtype, D) : nullptr;
+  if (split && !a.partials_out && !merge) return PKV_EUNSUPPORTED;
   // Split launches: the prep kernel orders the items longest first (natural order beyond
   // its item limit), then the decode grid, then the merge grid.  The two later grids are
   // launched with programmatic stream serialization: they may be scheduled before the grid
@@ -1219,7 +1223,7 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   cfg.attrs = ordered ? pdl : nullptr;
   cfg.numAttrs = ordered ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, fn, kmap, vmap, P) != cudaSuccess) return PKV_ECUDA;
-  if (split) {
+  if (merge) {
     const long long rows = static_cast<long long>(a.num_seqs) * a.num_q_heads;
     cudaLaunchConfig_t mcfg{};
     mcfg.gridDim = dim3(static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps));

@@ -30,6 +30,9 @@ struct DecodeArgs {
   unsigned* err;  // device error word
   bool kv_fp8;    // caches hold E4M3 codes (then k_scale / v_scale apply)
   float k_scale, v_scale;
+  // every context writes (m, l, o) partials to the workspace (layout of workspace_layout
+  // with partials = true) instead of `out`; no merge grid runs
+  bool partials_out;
 };
 
 // Resolved partition size in tokens, or -1 if `partition_size` is not acceptable.
@@ -42,8 +45,10 @@ struct WorkspaceLayout {
   size_t o_offset, ml_offset, order_offset, total;
   int max_parts;
 };
+// partials: lay the partials out even when no context can span two partitions.
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int block_size,
-                                 int max_blocks_per_seq, int partition_tokens);
+                                 int max_blocks_per_seq, int partition_tokens,
+                                 bool partials = false);
 
 // Whether the tensor-core path serves this shape (otherwise the CUDA-core path does).
 bool decode_uses_tensor_cores(pkv_dtype dtype, int head_dim, int block_size);
@@ -68,12 +73,47 @@ struct PrefillArgs {
   float scale;
   pkv_dtype dtype;
   unsigned* err;
+  // options of the tcgen05 kernel (zero / null for chunked prefill)
+  const int32_t* kv_start;    // per sequence, first attended position (a block multiple)
+  const int32_t* table_rows;  // per sequence, the block-table row it reads
+  bool non_causal;            // every row attends all of [kv_start, context_len)
+  float* part_o;              // write (m, l, o) partials instead of `out`
+  float* part_ml;
+  int ksplit;                 // key ranges per sequence, one partial each (non-causal)
 };
+
+// Whether the chunked-prefill kernel's tcgen05 path (the one with the options above)
+// serves this shape.
+bool prefill_umma_supported(pkv_dtype dtype, int head_dim, int block_size, int group,
+                            float scale);
 
 // Whether the chunked-prefill kernel serves this element type and shape.
 bool prefill_supported(pkv_dtype dtype, int head_dim, int block_size);
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+struct SharedPrefixArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* group_start;  // [num_groups + 1]: group g = sequences group_start[g] ..
+  const int32_t* prefix_lens;  // [num_groups]: shared prefix tokens (whole blocks)
+  int num_seqs, num_groups, max_group_size, max_prefix_tokens;
+  int num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks;
+  float scale;
+  pkv_dtype dtype;
+  void* workspace;
+  size_t workspace_bytes;
+  unsigned* err;
+};
+
+size_t shared_prefix_workspace_size(int num_seqs, int num_groups, int num_q_heads,
+                                    int num_kv_heads, int block_size, int max_blocks_per_seq,
+                                    int max_group_size, int max_prefix_tokens);
+int launch_shared_prefix(const SharedPrefixArgs& a, cudaStream_t stream);
 
 int launch_kv_cache_write_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
                               const int64_t* slot_mapping, int num_tokens, int row_elems,

@@ -53,6 +53,13 @@ struct PrefillParams {
   int num_seqs, num_q_tokens, num_q_heads, num_kv_heads, group, max_query_len;
   int max_blocks_per_seq, num_blocks, block_size, m_tiles, stages, stage_bytes;
   float scale_log2;
+  // Options of the tcgen05 kernel, used by the shared-prefix decode (all off for prefill):
+  const int32_t* kv_start;    // per sequence, first attended position (a block multiple), or null
+  const int32_t* table_rows;  // per sequence, the block-table row to read, or null (row s)
+  int causal;                 // 1: row i sees positions < L - n + i + 1; 0: every row sees < L
+  float* part_o;              // when set: unnormalised o [num_q_tokens, num_q_heads, 128] fp32
+  float* part_ml;             //   and (m in log2 units, l) [num_q_tokens, num_q_heads, 2]
+  int ksplit;                 // key ranges per sequence (non-causal only), one partial each
 };
 
 template <int ROWS>
@@ -392,6 +399,8 @@ __global__ void __launch_bounds__(kUThreads, 2)
   long long bid = blockIdx.x;
   const int g = static_cast<int>(bid % P.num_kv_heads);
   bid /= P.num_kv_heads;
+  const int split = static_cast<int>(bid % P.ksplit);
+  bid /= P.ksplit;
   const int mt = P.m_tiles - 1 - static_cast<int>(bid % P.m_tiles);
   const int s = static_cast<int>(bid / P.m_tiles);
   const int q0 = P.query_start[s], q1 = P.query_start[s + 1];
@@ -399,16 +408,40 @@ __global__ void __launch_bounds__(kUThreads, 2)
   const int L = P.context_lens[s];
   const int G = P.group;
   const int row0 = mt * kURows;
-  if (q0 < 0 || q1 > P.num_q_tokens || n < 0 || n > P.max_query_len || n > L ||
-      L > P.max_blocks_per_seq * P.block_size) {
+  const int ks0 = P.kv_start ? P.kv_start[s] : 0;  // first attended position
+  if (q0 < 0 || q1 > P.num_q_tokens || n < 0 || n > P.max_query_len ||
+      (P.causal && n > L) || L > P.max_blocks_per_seq * P.block_size || ks0 < 0 ||
+      ks0 % BS != 0) {
     if (tid == 0) raise_error(P.err, PKV_DERR_CONTEXT);
     return;
   }
   if (row0 >= n * G) return;
   const int rows = min(kURows, n * G - row0);
-  const int kmax = L - n + (row0 + rows - 1) / G;
-  const int ntiles = kmax / kUKeys + 1;
+  // key range of this split: whole 64-key tiles of [ks0, L), `split` of `ksplit`
+  const int span = ((max(L - ks0, 0) + kUKeys - 1) / kUKeys + P.ksplit - 1) / P.ksplit * kUKeys;
+  const int ks = ks0 + split * span;
+  const int ke = min(L, ks + span);  // one past the last key
+  float* part_o = P.part_o ? P.part_o + static_cast<size_t>(split) * P.num_q_tokens *
+                                            P.num_q_heads * 128
+                           : nullptr;
+  float* part_ml = P.part_ml ? P.part_ml + static_cast<size_t>(split) * P.num_q_tokens *
+                                              P.num_q_heads * 2
+                             : nullptr;
+  if (ks >= ke) {
+    // nothing to attend: the rows' partials are empty (m = -inf, l = 0, o = 0)
+    if (part_o && tid < rows) {
+      const int R = row0 + tid, i = R / G;
+      const size_t row = static_cast<size_t>(q0 + i) * P.num_q_heads + g * G + (R - i * G);
+      for (int d = 0; d < 128; ++d) part_o[row * 128 + d] = 0.f;
+      part_ml[row * 2] = -INFINITY;
+      part_ml[row * 2 + 1] = 0.f;
+    }
+    return;
+  }
+  const int kmax = P.causal ? L - n + (row0 + rows - 1) / G : ke - 1;
+  const int ntiles = (kmax - ks) / kUKeys + 1;
   const int live_blocks = (L + BS - 1) / BS;
+  const int blk0 = ks / BS;  // first block of tile 0
 
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sq = base;
@@ -470,7 +503,8 @@ __global__ void __launch_bounds__(kUThreads, 2)
     uint64_t* fullb = is_k ? k_full : v_full;
     uint64_t* emptyb = is_k ? k_empty : v_empty;
     const uint32_t tile_off = is_k ? 0u : static_cast<uint32_t>(kUTile);
-    const int32_t* bt = P.block_tables + static_cast<size_t>(s) * P.max_blocks_per_seq;
+    const int trow = P.table_rows ? P.table_rows[s] : s;
+    const int32_t* bt = P.block_tables + static_cast<size_t>(trow) * P.max_blocks_per_seq;
     const int x0 = g * D;
     if (lane == 0) {
       tma_prefetch_desc(map);
@@ -487,7 +521,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
       const int st = j % kUStages;
       int y = P.num_blocks * BS;
       if (lane < NBT) {
-        const int jb = j * NBT + lane;
+        const int jb = blk0 + j * NBT + lane;
         if (jb < live_blocks) {
           const int id = bt[jb];
           if (id >= 0 && id < P.num_blocks)
@@ -544,7 +578,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
       uint8_t* vt = ring + st * 2 * kUTile + kUTile;
       // value rows past the context (stale slots of the last block) become zeros before
       // they meet zero weights in P.V
-      const int vrows = L - i * kUKeys;
+      const int vrows = L - ks - i * kUKeys;
       if (vrows < kUKeys) {
         const int nz = (kUKeys - vrows) * 8;  // 16-byte chunks per box
         for (int e = lane; e < 2 * nz; e += 32) {
@@ -621,7 +655,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
     const int Rc = live ? R : n * G - 1;
     const int i = Rc / G;
     const int head = g * G + (Rc - i * G);
-    const int lim = L - n + i;
+    const int lim = (P.causal ? L - n + i : ke - 1) - ks;  // last key, relative to ks
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
     float m = -INFINITY, l = 0.f;
     int done = 0;
@@ -707,23 +741,45 @@ __global__ void __launch_bounds__(kUThreads, 2)
         if (lane == 0) fail();
       } else {
         tc_fence_after_sync();
-        const float inv = 1.f / l;
-        T* orow = static_cast<T*>(P.out) +
-                  (static_cast<size_t>(q0 + i) * P.num_q_heads + head) * D;
+        const size_t orow_i = static_cast<size_t>(q0 + i) * P.num_q_heads + head;
+        if (part_o) {
+          // the partial (m, l, o) of this key range, for a log-sum-exp merge
+          float* po = part_o + orow_i * D;
 #pragma unroll
-        for (int part = 0; part < D / 32; ++part) {
-          uint32_t ov[32];
-          tmem_ld32(tm_o + lane_off + part * 32, ov);
-          tmem_ld_wait();
+          for (int part = 0; part < D / 32; ++part) {
+            uint32_t ov[32];
+            tmem_ld32(tm_o + lane_off + part * 32, ov);
+            tmem_ld_wait();
+            if (live) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4*>(po + part * 32 + c) =
+                    make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
+                                __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
+            }
+          }
           if (live) {
+            part_ml[orow_i * 2] = m;
+            part_ml[orow_i * 2 + 1] = l;
+          }
+        } else {
+          const float inv = 1.f / l;
+          T* orow = static_cast<T*>(P.out) + orow_i * D;
 #pragma unroll
-            for (int c = 0; c < 32; c += 8) {
-              uint4 v;
-              v.x = Mma<T>::pack(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-              v.y = Mma<T>::pack(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
-              v.z = Mma<T>::pack(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
-              v.w = Mma<T>::pack(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + part * 32 + c) = v;
+          for (int part = 0; part < D / 32; ++part) {
+            uint32_t ov[32];
+            tmem_ld32(tm_o + lane_off + part * 32, ov);
+            tmem_ld_wait();
+            if (live) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 v;
+                v.x = Mma<T>::pack(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
+                v.y = Mma<T>::pack(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
+                v.z = Mma<T>::pack(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
+                v.w = Mma<T>::pack(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
+                *reinterpret_cast<uint4*>(orow + part * 32 + c) = v;
+              }
             }
           }
         }
@@ -843,6 +899,12 @@ bool prefill_supported(pkv_dtype dtype, int head_dim, int block_size) {
          (block_size == 16 || block_size == 32 || block_size == 64);
 }
 
+bool prefill_umma_supported(pkv_dtype dtype, int head_dim, int block_size, int group,
+                            float scale) {
+  return prefill_supported(dtype, head_dim, block_size) && umma_path(head_dim, group) &&
+         scale > 0.f;
+}
+
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (!prefill_supported(a.dtype, a.head_dim, a.block_size)) return PKV_EUNSUPPORTED;
   if (a.num_seqs == 0 || a.num_q_tokens == 0 || a.max_query_len == 0) return PKV_OK;
@@ -871,7 +933,17 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   P.stage_bytes = 2 * kKeyTile * D * 2;
   P.stages = D == 128 ? 3 : 4;
   P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  const long long grid = static_cast<long long>(a.num_seqs) * P.m_tiles * a.num_kv_heads;
+  P.kv_start = a.kv_start;
+  P.table_rows = a.table_rows;
+  P.causal = a.non_causal ? 0 : 1;
+  P.part_o = a.part_o;
+  P.part_ml = a.part_ml;
+  P.ksplit = a.ksplit > 0 ? a.ksplit : 1;
+  const bool options = a.kv_start || a.table_rows || a.non_causal || a.part_o || P.ksplit > 1;
+  if (options && (!umma || (P.ksplit > 1 && P.causal) || (!a.part_o && P.ksplit > 1)))
+    return PKV_EUNSUPPORTED;
+  const long long grid =
+      static_cast<long long>(a.num_seqs) * P.m_tiles * a.num_kv_heads * P.ksplit;
   if (grid > INT_MAX) return PKV_EUNSUPPORTED;
   const int smem = 1024 + P.stages * P.stage_bytes + 16 * P.stages + 16;
   if (smem > kMaxPrefillSmem) return PKV_EUNSUPPORTED;

@@ -314,6 +314,60 @@ def prefill_workload(*, seed: int = BASE_SEED + 6, num_seqs: int = 16, chunk: in
                                  max_blocks_per_seq=(max_prior + chunk + 15) // 16)
 
 
+def grouped_prefix_workload(*, seed: int = BASE_SEED + 7, groups: int = 64, members: int = 8,
+                            prefix_tokens: int = 4096, suffix_range=(1, 256), num_q_heads: int = 32,
+                            num_kv_heads: int = 8, head_dim: int = 128, block_size: int = 16,
+                            dtype: str = "bf16") -> Workload:
+    """Groups of sequences forked from one prompt each (parallel sampling, beam search).
+
+    Group g's members are consecutive sequences whose first ``prefix_tokens`` (whole
+    blocks) map the group's own physical prefix blocks; each member then owns a suffix of
+    U[suffix_range] tokens in private blocks.  ``info`` holds ``group_start`` and
+    ``prefix_lens`` (the shared-prefix description of the batch).
+    """
+    if prefix_tokens % block_size:
+        raise ValueError("prefix_tokens must be whole blocks")
+    ss = np.random.SeedSequence(seed)
+    s_q, s_k, s_v, s_perm, s_len = ss.spawn(5)
+    bs = block_size
+    B = groups * members
+    g = np.random.Generator(np.random.PCG64(s_len))
+    suffix = g.integers(suffix_range[0], suffix_range[1], size=B, endpoint=True)
+    lens = (prefix_tokens + suffix).astype(np.int32)
+    pre_blocks = prefix_tokens // bs
+    own = [_blocks_for(int(x), bs) for x in suffix]
+    need = groups * pre_blocks + int(sum(own))
+    NB = math.ceil(1.1 * need)
+    perm = np.random.Generator(np.random.PCG64(s_perm)).permutation(NB).astype(np.int32)
+    MB = pre_blocks + _blocks_for(suffix_range[1], bs)
+    bt = np.full((B, MB), -1, dtype=np.int32)
+    nxt = 0
+    for gi in range(groups):
+        ids = perm[nxt:nxt + pre_blocks]
+        nxt += pre_blocks
+        for m in range(members):
+            s = gi * members + m
+            bt[s, :pre_blocks] = ids
+            bt[s, pre_blocks:pre_blocks + own[s]] = perm[nxt:nxt + own[s]]
+            nxt += own[s]
+    q = normal_storage(s_q, (B, num_q_heads, head_dim), dtype)
+    k = normal_storage(s_k, (NB, bs, num_kv_heads, head_dim), dtype)
+    v = normal_storage(s_v, (NB, bs, num_kv_heads, head_dim), dtype)
+    return Workload(name=f"grouped-prefix-{groups}x{members}-p{prefix_tokens}-{dtype}", dtype=dtype,
+                    num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                    block_size=bs, scale=1.0 / math.sqrt(head_dim), q=q, k_cache=k, v_cache=v,
+                    block_tables=bt, context_lens=lens,
+                    info={"seed": seed, "group_start": np.arange(0, B + 1, members, dtype=np.int32),
+                          "prefix_lens": np.full(groups, prefix_tokens, dtype=np.int32),
+                          "shared_prefix_tokens": prefix_tokens, "pool_blocks_needed": need})
+
+
+GROUPED_PREFIX_RECIPE = ("grouped shared prefixes bf16: 64 groups x 8 sequences (parallel "
+                         "sampling), each group sharing a 4096-token prompt in 256 physical "
+                         "blocks, private suffixes uniform in [1,256] tokens, 32 q heads over 8 KV "
+                         "heads, head_dim 128, block_size 16, shuffled pool sized to need + 10%")
+
+
 # ---------------------------------------------------------------------------------------
 # the five decode batches
 # ---------------------------------------------------------------------------------------
@@ -430,7 +484,9 @@ def shared_prefix_workload(*, seed: int, num_seqs: int = 256, prefix_tokens: int
                  scale=1.0 / math.sqrt(head_dim), q=q, k_cache=k, v_cache=v, block_tables=bt,
                  context_lens=lens,
                  info={"seed": seed, "prefix_tokens": prefix_tokens, "shared_blocks": shared,
-                       "shared_ids": shared_ids.copy(), "pool_blocks_needed": need})
+                       "shared_ids": shared_ids.copy(), "pool_blocks_needed": need,
+                       # tokens in the blocks every sequence still maps after its copy
+                       "shared_prefix_tokens": (shared - (1 if prefix_partial else 0)) * bs})
     if with_writes:
         n = len(slots)
         w.slot_mapping = np.asarray(slots, dtype=np.int64)

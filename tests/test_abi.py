@@ -98,6 +98,20 @@ def test_argument_checks_return_before_any_cuda_call(lib):
     assert p(*pargs(8, 4, 128, 8, 1, 4)) == -4      # block_size not served
     assert p(*pargs(8, 4, 128, 16, 1, 0)) == 0      # no query rows: nothing to do
     assert p(*pargs(8, 4, 128, 16, 1, 4)) == -1     # null pointers
+    sp = lib.paged_attn_decode_shared_prefix
+    sp.restype = ctypes.c_int
+    spargs = lambda hq, hkv, d, bs, dt, scale: (  # noqa: E731
+        null, null, null, null, null, null, null, null, ctypes.c_int(4), ctypes.c_int(1),
+        ctypes.c_int(4), ctypes.c_int(64), ctypes.c_int(hq), ctypes.c_int(hkv), ctypes.c_int(d),
+        ctypes.c_int(bs), ctypes.c_int(8), ctypes.c_int(16), ctypes.c_float(scale),
+        ctypes.c_int(dt), null, ctypes.c_size_t(0), null)
+    assert sp(*spargs(8, 2, 64, 16, 1, 0.1)) == -4     # head_dim 64 not served
+    assert sp(*spargs(12, 4, 128, 16, 1, 0.1)) == -4   # 3 heads per KV head not served
+    assert sp(*spargs(8, 2, 128, 16, 1, -0.1)) == -4   # negative scale not served
+    assert sp(*spargs(8, 2, 128, 16, 1, 0.1)) == -1    # null pointers
+    ws = lib.paged_attn_decode_shared_prefix_workspace_size
+    ws.restype = ctypes.c_size_t
+    assert ws(256, 1, 32, 8, 32, 48, 256, 992) >= 2 * 256 * 32 * 130 * 4
 
 
 def test_default_partition_size_follows_available_parallelism(lib):
