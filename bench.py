@@ -44,14 +44,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # beside it (profiles/ holds the captures).
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each
-    "13b-mha-b64-bf16@2048": {"bytes": 1408829696 + 3771392, "decode_cu_sha": "b4833870dd0161af"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963545600 + 6620416, "decode_cu_sha": "b4833870dd0161af"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328524800 + 4629248, "decode_cu_sha": "b4833870dd0161af"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4295690240 + 35983872, "decode_cu_sha": "b4833870dd0161af"},
-    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704843008 + 3724288, "decode_cu_sha": "b4833870dd0161af"},
-    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483319296 + 5715968, "decode_cu_sha": "b4833870dd0161af"},
-    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164936448 + 4075264, "decode_cu_sha": "b4833870dd0161af"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148132352 + 34985216, "decode_cu_sha": "b4833870dd0161af"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408804352 + 3820032, "decode_cu_sha": "047b90154d7d2fba"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963510272 + 6449920, "decode_cu_sha": "047b90154d7d2fba"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328517888 + 4689408, "decode_cu_sha": "047b90154d7d2fba"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4295699712 + 35980032, "decode_cu_sha": "047b90154d7d2fba"},
+    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704761088 + 3767808, "decode_cu_sha": "047b90154d7d2fba"},
+    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483313152 + 5967104, "decode_cu_sha": "047b90154d7d2fba"},
+    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164918016 + 4063744, "decode_cu_sha": "047b90154d7d2fba"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148135680 + 35195904, "decode_cu_sha": "047b90154d7d2fba"},
 }
 
 
@@ -649,7 +649,7 @@ def run_swap(args) -> None:
 
 # DRAM bytes (read + write) per launch of the chunked-prefill kernel on the chunked-prefill
 # batch, from one ncu capture, valid only for the kernel source whose hash is recorded.
-PREFILL_TRAFFIC = {"bytes": 278724864 + 106318080, "prefill_cu_sha": "9bd66ea7247fc2e3"}
+PREFILL_TRAFFIC = {"bytes": 278732800 + 106139392, "prefill_cu_sha": "e46532b8844fa6c1"}
 
 
 def prefill_traffic() -> float | None:
