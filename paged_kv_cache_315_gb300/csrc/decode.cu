@@ -45,6 +45,7 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kTcHeads = 16;    // query heads per CTA on the tensor-core path
+constexpr int kFp8gHeads = 8;   // ... on the fp8 path with heads in the MMA's N dimension
 constexpr int kSimtHeads = 8;   // ... on the CUDA-core path
 constexpr int kMaxStageSet = 4; // stages per warp, at most
 constexpr int kMaxParts = 1024; // partitions per sequence, at most
@@ -826,6 +827,227 @@ KernelFn simt_kernel_for(int D) {
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// fp8 decode with the query heads in the N dimension (at most 8 query heads per KV head)
+// ------------------------------------------------------------------------------------------
+//
+// S^T = K . Q^T (M = 16 tokens per m-tile, N = 8 heads, K = head_dim) and
+// O^T += V^T . P^T (M = head_dim in 8 m-tiles, N = 8 heads, K = 16 tokens per step), so no
+// MMA row is spent on absent heads and each thread owns whole columns (heads 2c, 2c+1).
+//   - K as the A operand: lane (r8, c) holds tokens r8 and r8 + 8 of an m-tile; head_dim is
+//     visited in the permuted order of the other fp8 kernel (lane c owns bytes [32c, 32c+32)
+//     of a row), shared with Q's B fragments.
+//   - V^T as the A operand: row r8 (and r8 + 8) of m-tile mt is head_dim element 16 r8 + 2 mt
+//     (and + 1), so a lane reads one 16-byte chunk per token row and pairs tokens with byte
+//     permutes (prmt) before the e4m3 -> f16 conversion.  The epilogue undoes the order.
+//   - P^T as the B operand: two movmatrix transposes per 16 tokens.
+template <int TR>
+__device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint32_t (&qb)[8][2],
+                                           float (&o)[8][4], float (&m)[2], float (&l)[2],
+                                           int valid, float scale_log2, int lane) {
+  constexpr int MT = TR / 16;
+  const int c = lane & 3, r8 = lane >> 2;
+  float sc[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+    const int ra = mt * 16 + r8, rb = ra + 8;
+    const uint4 a0 = lds128(kb + swz_chunk(ra, 2 * c)), a1 = lds128(kb + swz_chunk(ra, 2 * c + 1));
+    const uint4 b0 = lds128(kb + swz_chunk(rb, 2 * c)), b1 = lds128(kb + swz_chunk(rb, 2 * c + 1));
+    const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t fa[4];
+      e4m3x4_to_f16x2x2(wa[kk], fa[0], fa[2]);
+      e4m3x4_to_f16x2x2(wb[kk], fa[1], fa[3]);
+      Mma<__half>::run(sc[mt], fa, qb[kk][0], qb[kk][1]);
+    }
+  }
+  // online softmax per head (column): tokens past `valid` are masked
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int tok = mt * 16 + r8 + (e >> 1) * 8;
+      const float v = sc[mt][e] * scale_log2;
+      sc[mt][e] = tok < valid ? v : -INFINITY;
+    }
+    mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
+    mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
+  }
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const bool up0 = mx0 > m[0] + kRescaleSlack, up1 = mx1 > m[1] + kRescaleSlack;
+  const float mn0 = up0 ? mx0 : m[0], mn1 = up1 ? mx1 : m[1];
+  uint32_t pb[MT][2];
+  float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const uint32_t lo = Mma<__half>::pack(exp2f(sc[mt][0] - mn0), exp2f(sc[mt][1] - mn1));
+    const uint32_t hi = Mma<__half>::pack(exp2f(sc[mt][2] - mn0), exp2f(sc[mt][3] - mn1));
+    const float2 flo = Mma<__half>::unpack(lo), fhi = Mma<__half>::unpack(hi);
+    rs0 += flo.x + fhi.x;
+    rs1 += flo.y + fhi.y;
+    pb[mt][0] = movmatrix_trans(lo);  // (head r8, tokens 2c, 2c + 1)
+    pb[mt][1] = movmatrix_trans(hi);  // (head r8, tokens 8 + 2c, 9 + 2c)
+  }
+  if (__any_sync(0xffffffffu, up0 || up1)) {
+    const float a0 = exp2f(m[0] - mn0), a1 = exp2f(m[1] - mn1);  // 1 for heads that kept m
+    l[0] *= a0;
+    l[1] *= a1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= a0;
+      o[mt][1] *= a1;
+      o[mt][2] *= a0;
+      o[mt][3] *= a1;
+    }
+  }
+  m[0] = mn0;
+  m[1] = mn1;
+  l[0] += rs0;
+  l[1] += rs1;
+  // O^T += V^T . P^T
+#pragma unroll
+  for (int kt = 0; kt < MT; ++kt) {
+    const int t0 = kt * 16 + 2 * c;
+    const uint4 x0 = lds128(vb + swz_chunk(t0, r8)), x1 = lds128(vb + swz_chunk(t0 + 1, r8));
+    const uint4 x2 = lds128(vb + swz_chunk(t0 + 8, r8)), x3 = lds128(vb + swz_chunk(t0 + 9, r8));
+    const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
+    const uint32_t w2[4] = {x2.x, x2.y, x2.z, x2.w}, w3[4] = {x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+      // head_dim 16 r8 + 4 qd + e, e = 0..3, for the token pairs (t0, t0+1) and (t0+8, t0+9)
+      uint32_t p[4], q[4];
+      e4m3x4_to_f16x2x2(__byte_perm(w0[qd], w1[qd], 0x5140), p[0], p[1]);
+      e4m3x4_to_f16x2x2(__byte_perm(w0[qd], w1[qd], 0x7362), p[2], p[3]);
+      e4m3x4_to_f16x2x2(__byte_perm(w2[qd], w3[qd], 0x5140), q[0], q[1]);
+      e4m3x4_to_f16x2x2(__byte_perm(w2[qd], w3[qd], 0x7362), q[2], q[3]);
+      const uint32_t fa0[4] = {p[0], p[1], q[0], q[1]};  // m-tile 2 qd
+      const uint32_t fa1[4] = {p[2], p[3], q[2], q[3]};  // m-tile 2 qd + 1
+      Mma<__half>::run(o[2 * qd], fa0, pb[kt][0], pb[kt][1]);
+      Mma<__half>::run(o[2 * qd + 1], fa1, pb[kt][0], pb[kt][1]);
+    }
+  }
+}
+
+template <typename T, int BS, int PAIR>
+__global__ void __launch_bounds__(kThreads)
+    decode_fp8g_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap, const Params P) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  Work w;
+  int spec_id;
+  if (!decode_work<T>(P, D, w, spec_id)) return;
+  const Smem sm = carve(smem_raw, P);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int x0 = w.g * D;  // bytes of one KV head's row segment
+  pipeline_start(P, w, sm, &kmap, &vmap, x0, spec_id);
+
+  // Q^T B fragments in fp16: head r8, head_dim 32c + 4kk + (0, 1) and (2, 3)
+  uint32_t qb[8][2];
+  {
+    const int r8 = lane >> 2, c = lane & 3;
+    const T* qs = static_cast<const T*>(P.q) +
+                  (static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r8) * D;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int d0 = 32 * c + 4 * kk;
+      qb[kk][0] = r8 < w.hc ? to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qs + d0)), T()) : 0u;
+      qb[kk][1] =
+          r8 < w.hc ? to_f16x2(__ldg(reinterpret_cast<const uint32_t*>(qs + d0 + 2)), T()) : 0u;
+    }
+  }
+  constexpr int TR = BS * PAIR;  // token rows of a staged tile
+  const int nv = (w.nblk + PAIR - 1) / PAIR;
+  const int vpp = P.partition_blocks / PAIR;  // staged tiles per partition
+  bool dead = false;
+  float o[8][4];
+  float m[2], l[2];
+  for (int k = 0; k < w.nparts; ++k) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+    const int ve = min(nv, (k + 1) * vpp);
+    for (int v = k * vpp + warp; v < ve && !dead; v += kWarps) {
+      const int st = v % P.stages;
+      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (v / P.stages) & 1)) {
+        if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
+        drain_after_timeout(P, w, sm, v);
+        dead = true;
+        break;
+      }
+      uint8_t* ktile = sm.ring + st * P.stage_bytes;
+      uint8_t* vtile = ktile + P.tile_stride;
+      const int valid = min(TR, w.tok_valid - v * TR);
+      if (valid < TR) {
+        zero_tail_rows<64, TR>(vtile, valid, lane);  // 128-byte rows, one box
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      fp8g_block<TR>(smem_addr(ktile), smem_addr(vtile), qb, o, m, l, valid, P.scale_log2, lane);
+      __syncwarp();
+      if (lane == 0 && v + P.stages < nv) issue_tile(P, sm, &kmap, &vmap, v + P.stages, x0, w.nblk);
+    }
+
+    __syncthreads();
+    const int HC = P.head_chunk;
+    float* O_s = sm.merge;
+    float* ml_s = O_s + kWarps * HC * D;
+    {
+      const int r8 = lane >> 2, c = lane & 3;
+      const int h0 = 2 * c, h1 = 2 * c + 1;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int d = 16 * r8 + 2 * mt;  // rows r8 and r8 + 8 of m-tile mt: d and d + 1
+        if (h0 < w.hc) {
+          O_s[(warp * HC + h0) * D + d] = o[mt][0];
+          O_s[(warp * HC + h0) * D + d + 1] = o[mt][2];
+        }
+        if (h1 < w.hc) {
+          O_s[(warp * HC + h1) * D + d] = o[mt][1];
+          O_s[(warp * HC + h1) * D + d + 1] = o[mt][3];
+        }
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+      }
+      if (r8 == 0) {
+        if (h0 < w.hc) {
+          ml_s[(warp * HC + h0) * 2] = m[0];
+          ml_s[(warp * HC + h0) * 2 + 1] = l[0];
+        }
+        if (h1 < w.hc) {
+          ml_s[(warp * HC + h1) * 2] = m[1];
+          ml_s[(warp * HC + h1) * 2 + 1] = l[1];
+        }
+      }
+    }
+    __syncthreads();
+    Work wk = w;
+    wk.p = w.p + k;
+    finish<T>(P, wk, D, HC, O_s, ml_s);
+    if (k + 1 < w.nparts) __syncthreads();
+  }
+}
+
+template <typename T>
+KernelFn fp8g_kernel_for(int BS) {
+  if (BS == 16) return decode_fp8g_kernel<T, 16, 2>;
+  if (BS == 32) return decode_fp8g_kernel<T, 32, 1>;
+  if (BS == 64) return decode_fp8g_kernel<T, 64, 1>;
+  return nullptr;
+}
+
 template <typename T>
 KernelFn fp8_kernel_for(int BS) {
   if (BS == 16) return decode_fp8_kernel<T, 16, 2>;  // two 16-token blocks per staged tile
@@ -1130,6 +1352,8 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   P.num_q_heads = a.num_q_heads;
   P.num_kv_heads = a.num_kv_heads;
   P.group = a.num_q_heads / a.num_kv_heads;
+  // fp8 caches with at most 8 query heads per KV head: the kernel with heads in N
+  const bool fp8g = a.kv_fp8 && P.group <= kFp8gHeads;
   P.head_chunk = std::min(P.group, tc ? kTcHeads : kSimtHeads);
   P.num_chunks = (P.group + P.head_chunk - 1) / P.head_chunk;
   P.max_blocks_per_seq = a.max_blocks_per_seq;
@@ -1182,9 +1406,11 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
                       BS, tc))
     return PKV_ECUDA;
 
-  KernelFn fn = a.kv_fp8 ? (a.dtype == PKV_BF16 ? fp8_kernel_for<__nv_bfloat16>(BS)
+  KernelFn fn = fp8g     ? (a.dtype == PKV_BF16 ? fp8g_kernel_for<__nv_bfloat16>(BS)
+                                                : fp8g_kernel_for<__half>(BS))
+                : a.kv_fp8 ? (a.dtype == PKV_BF16 ? fp8_kernel_for<__nv_bfloat16>(BS)
                                                 : fp8_kernel_for<__half>(BS))
-                         : kernel_for(a.dtype, D, BS, tc);
+                           : kernel_for(a.dtype, D, BS, tc);
   if (!fn) return PKV_EUNSUPPORTED;
   const bool split = wl.total > 0;
   // with partials_out the caller merges the partials itself
