@@ -44,14 +44,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # beside it (profiles/ holds the captures).
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each
-    "13b-mha-b64-bf16@2048": {"bytes": 1408804352 + 3820032, "decode_cu_sha": "047b90154d7d2fba"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963510272 + 6449920, "decode_cu_sha": "047b90154d7d2fba"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328517888 + 4689408, "decode_cu_sha": "047b90154d7d2fba"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4295699712 + 35980032, "decode_cu_sha": "047b90154d7d2fba"},
-    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704761088 + 3767808, "decode_cu_sha": "047b90154d7d2fba"},
-    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483313152 + 5967104, "decode_cu_sha": "047b90154d7d2fba"},
-    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164918016 + 4063744, "decode_cu_sha": "047b90154d7d2fba"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148135680 + 35195904, "decode_cu_sha": "047b90154d7d2fba"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408830208 + 3778560, "decode_cu_sha": "319b66ed338144c4"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963482368 + 6345984, "decode_cu_sha": "319b66ed338144c4"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328503040 + 4684544, "decode_cu_sha": "319b66ed338144c4"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4295698688 + 35986432, "decode_cu_sha": "319b66ed338144c4"},
+    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704768512 + 9554176, "decode_cu_sha": "319b66ed338144c4"},
+    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483278592 + 8974336, "decode_cu_sha": "319b66ed338144c4"},
+    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 165059840 + 5685248, "decode_cu_sha": "319b66ed338144c4"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2160471552 + 55312128, "decode_cu_sha": "319b66ed338144c4"},
 }
 
 

@@ -937,7 +937,7 @@ __device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint3
 }
 
 template <typename T, int BS, int PAIR>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 5)
     decode_fp8g_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap vmap, const Params P) {
   constexpr int D = 128;
@@ -1242,12 +1242,15 @@ struct Geometry {
 };
 
 Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, int max_parts,
-                  bool fp8 = false, int pair = 1, int ppc = 1, int head_chunk = 0) {
+                  bool fp8 = false, int pair = 1, int ppc = 1, int head_chunk = 0,
+                  bool shallow = false) {
   Geometry g{};
   g.tile_bytes = BS * D * (fp8 ? 1 : static_cast<int>(dtype_size(dt)));
   g.tile_stride = static_cast<int>(align_up(static_cast<size_t>(pair) * g.tile_bytes, 1024));
   g.stage_bytes = 2 * g.tile_stride;
-  const int per_warp = std::max(1, std::min(kMaxStageSet, 16384 / g.stage_bytes));
+  // (shallow: the heads-in-N fp8 kernel runs five CTAs per SM on half the stages)
+  const int per_warp =
+      std::max(1, std::min(kMaxStageSet, (shallow ? 8192 : 16384) / g.stage_bytes));
   g.stages = kWarps * per_warp;
   const int HC = tc ? kTcHeads : kSimtHeads;
   const size_t epi = (static_cast<size_t>(kWarps) * HC * D + kWarps * HC * 2) * sizeof(float);
@@ -1374,12 +1377,12 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (tc && a.partition_tokens < 1024 && P.head_chunk <= 4 && wl.max_parts > 1 &&
       P.partition_blocks % (4 * P.pair) == 0) {
     const Geometry g2 = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
-                                 P.pair, 2, P.head_chunk);
-    if (3 * (g2.smem_bytes + 1024) <= 228 * 1024) P.ppc = 2;
+                                 P.pair, 2, P.head_chunk, fp8g);
+    if ((fp8g ? 5 : 3) * (g2.smem_bytes + 1024) <= 228 * 1024) P.ppc = 2;
   }
   P.max_groups = (wl.max_parts + P.ppc - 1) / P.ppc;
   const Geometry g = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
-                              P.pair, P.ppc, P.head_chunk);
+                              P.pair, P.ppc, P.head_chunk, fp8g);
   P.merge_off = g.merge_off;
   if (g.smem_bytes > kMaxSmem) return PKV_EUNSUPPORTED;
   P.stages = g.stages;
