@@ -828,6 +828,202 @@ KernelFn simt_kernel_for(int D) {
 }
 
 // ------------------------------------------------------------------------------------------
+// 16-bit decode with the query heads in the N dimension (head_dim 128, at most 8 heads)
+// ------------------------------------------------------------------------------------------
+//
+// S^T = K . Q^T (M = 16 tokens per m-tile, N = 8 heads, K = head_dim) and
+// O^T += V^T . P^T (M = head_dim in 8 m-tiles, N = 8 heads, K = 16 tokens per step).  K
+// enters as the A operand through ldmatrix, V^T through ldmatrix.trans, and P^T through two
+// movmatrix transposes per 16 tokens; Q^T's B fragments stay in registers.  Half the
+// accumulator and Q registers of the M = heads layout, so more CTAs fit on an SM.
+template <typename T, int BS>
+__device__ __forceinline__ void tcg_block(uint32_t kb, uint32_t vb, const uint32_t (&qb)[8][2],
+                                          float (&o)[8][4], float (&m)[2], float (&l)[2],
+                                          int valid, float scale_log2, int lane) {
+  constexpr int MT = BS / 16;
+  const int c = lane & 3, r8 = lane >> 2;
+  float sc[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
+    // A fragment rows: token mt*16 + (lane & 7) + 8 * ((lane >> 3) & 1), cols +8 for lanes 16-31
+    const int r = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(kb + swz<BS>(r, kk * 16 + (lane >> 4) * 8), a[0], a[1], a[2], a[3]);
+      Mma<T>::run(sc[mt], a, qb[kk][0], qb[kk][1]);
+    }
+  }
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int tok = mt * 16 + r8 + (e >> 1) * 8;
+      const float v = sc[mt][e] * scale_log2;
+      sc[mt][e] = tok < valid ? v : -INFINITY;
+    }
+    mx0 = fmaxf(mx0, fmaxf(sc[mt][0], sc[mt][2]));
+    mx1 = fmaxf(mx1, fmaxf(sc[mt][1], sc[mt][3]));
+  }
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const bool up0 = mx0 > m[0] + kRescaleSlack, up1 = mx1 > m[1] + kRescaleSlack;
+  const float mn0 = up0 ? mx0 : m[0], mn1 = up1 ? mx1 : m[1];
+  uint32_t pb[MT][2];
+  float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const uint32_t lo = Mma<T>::pack(exp2f(sc[mt][0] - mn0), exp2f(sc[mt][1] - mn1));
+    const uint32_t hi = Mma<T>::pack(exp2f(sc[mt][2] - mn0), exp2f(sc[mt][3] - mn1));
+    const float2 flo = Mma<T>::unpack(lo), fhi = Mma<T>::unpack(hi);
+    rs0 += flo.x + fhi.x;
+    rs1 += flo.y + fhi.y;
+    pb[mt][0] = movmatrix_trans(lo);  // (head r8, tokens 2c, 2c + 1)
+    pb[mt][1] = movmatrix_trans(hi);  // (head r8, tokens 8 + 2c, 9 + 2c)
+  }
+  if (__any_sync(0xffffffffu, up0 || up1)) {
+    const float a0 = exp2f(m[0] - mn0), a1 = exp2f(m[1] - mn1);
+    l[0] *= a0;
+    l[1] *= a1;
+#pragma unroll
+    for (int md = 0; md < 8; ++md) {
+      o[md][0] *= a0;
+      o[md][1] *= a1;
+      o[md][2] *= a0;
+      o[md][3] *= a1;
+    }
+  }
+  m[0] = mn0;
+  m[1] = mn1;
+  l[0] += rs0;
+  l[1] += rs1;
+  // O^T += V^T . P^T: A fragments of V^T (rows d, cols tokens) by transposing loads of V
+#pragma unroll
+  for (int kt = 0; kt < MT; ++kt) {
+    const int r = kt * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
+#pragma unroll
+    for (int md = 0; md < 8; ++md) {
+      uint32_t a[4];
+      ldsm_x4_trans(vb + swz<BS>(r, md * 16 + ((lane >> 3) & 1) * 8), a[0], a[1], a[2], a[3]);
+      Mma<T>::run(o[md], a, pb[kt][0], pb[kt][1]);
+    }
+  }
+}
+
+template <typename T, int BS>
+__global__ void __launch_bounds__(kThreads, 5)
+    decode_tcg_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const Params P) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  Work w;
+  int spec_id;
+  if (!decode_work<T>(P, D, w, spec_id)) return;
+  const Smem sm = carve(smem_raw, P);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int x0 = w.g * D;
+  pipeline_start(P, w, sm, &kmap, &vmap, x0, spec_id);
+
+  // Q^T B fragments: head r8, head_dim kk*16 + 2c (+1) and kk*16 + 8 + 2c (+1)
+  uint32_t qb[8][2];
+  {
+    const int r8 = lane >> 2, c = lane & 3;
+    const T* qs = static_cast<const T*>(P.q) +
+                  (static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r8) * D;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int d0 = kk * 16 + 2 * c;
+      qb[kk][0] = r8 < w.hc ? __ldg(reinterpret_cast<const uint32_t*>(qs + d0)) : 0u;
+      qb[kk][1] = r8 < w.hc ? __ldg(reinterpret_cast<const uint32_t*>(qs + d0 + 8)) : 0u;
+    }
+  }
+  bool dead = false;
+  float o[8][4];
+  float m[2], l[2];
+  for (int k = 0; k < w.nparts; ++k) {
+#pragma unroll
+    for (int md = 0; md < 8; ++md) o[md][0] = o[md][1] = o[md][2] = o[md][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+    const int je = min(w.nblk, (k + 1) * P.partition_blocks);
+    for (int j = k * P.partition_blocks + warp; j < je && !dead; j += kWarps) {
+      const int st = j % P.stages;
+      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (j / P.stages) & 1)) {
+        if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
+        drain_after_timeout(P, w, sm, j);
+        dead = true;
+        break;
+      }
+      uint8_t* ktile = sm.ring + st * P.stage_bytes;
+      uint8_t* vtile = ktile + P.tile_stride;
+      const int valid = min(BS, w.tok_valid - j * BS);
+      if (valid < BS) {
+        zero_tail_rows<D, BS>(vtile, valid, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tcg_block<T, BS>(smem_addr(ktile), smem_addr(vtile), qb, o, m, l, valid, P.scale_log2, lane);
+      __syncwarp();
+      if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0, w.nblk);
+    }
+
+    __syncthreads();
+    const int HC = P.head_chunk;
+    float* O_s = sm.merge;
+    float* ml_s = O_s + kWarps * HC * D;
+    {
+      const int r8 = lane >> 2, c = lane & 3;
+      const int h0 = 2 * c, h1 = 2 * c + 1;
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        const int d = md * 16 + r8;
+        if (h0 < w.hc) {
+          O_s[(warp * HC + h0) * D + d] = o[md][0];
+          O_s[(warp * HC + h0) * D + d + 8] = o[md][2];
+        }
+        if (h1 < w.hc) {
+          O_s[(warp * HC + h1) * D + d] = o[md][1];
+          O_s[(warp * HC + h1) * D + d + 8] = o[md][3];
+        }
+      }
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+      }
+      if (r8 == 0) {
+        if (h0 < w.hc) {
+          ml_s[(warp * HC + h0) * 2] = m[0];
+          ml_s[(warp * HC + h0) * 2 + 1] = l[0];
+        }
+        if (h1 < w.hc) {
+          ml_s[(warp * HC + h1) * 2] = m[1];
+          ml_s[(warp * HC + h1) * 2 + 1] = l[1];
+        }
+      }
+    }
+    __syncthreads();
+    Work wk = w;
+    wk.p = w.p + k;
+    finish<T>(P, wk, D, HC, O_s, ml_s);
+    if (k + 1 < w.nparts) __syncthreads();
+  }
+}
+
+template <typename T>
+KernelFn tcg_kernel_for(int BS) {
+  if (BS == 16) return decode_tcg_kernel<T, 16>;
+  if (BS == 32) return decode_tcg_kernel<T, 32>;
+  if (BS == 64) return decode_tcg_kernel<T, 64>;
+  return nullptr;
+}
+
+// ------------------------------------------------------------------------------------------
 // fp8 decode with the query heads in the N dimension (at most 8 query heads per KV head)
 // ------------------------------------------------------------------------------------------
 //
@@ -1248,7 +1444,7 @@ Geometry geometry(pkv_dtype dt, int D, int BS, bool tc, int partition_blocks, in
   g.tile_bytes = BS * D * (fp8 ? 1 : static_cast<int>(dtype_size(dt)));
   g.tile_stride = static_cast<int>(align_up(static_cast<size_t>(pair) * g.tile_bytes, 1024));
   g.stage_bytes = 2 * g.tile_stride;
-  // (shallow: the heads-in-N fp8 kernel runs five CTAs per SM on half the stages)
+  // (shallow: the heads-in-N kernels run five CTAs per SM on half the stages)
   const int per_warp =
       std::max(1, std::min(kMaxStageSet, (shallow ? 8192 : 16384) / g.stage_bytes));
   g.stages = kWarps * per_warp;
@@ -1357,6 +1553,10 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   P.group = a.num_q_heads / a.num_kv_heads;
   // fp8 caches with at most 8 query heads per KV head: the kernel with heads in N
   const bool fp8g = a.kv_fp8 && P.group <= kFp8gHeads;
+  // 16-bit caches, head_dim 128, 2 to 8 query heads per KV head (GQA): heads in N as well.
+  // (With one head per KV head the deeper ring of the M = heads kernel streams faster.)
+  const bool tcg = !a.kv_fp8 && tc && D == 128 && P.group >= 2 && P.group <= kFp8gHeads;
+  const bool shallow = fp8g || tcg;
   P.head_chunk = std::min(P.group, tc ? kTcHeads : kSimtHeads);
   P.num_chunks = (P.group + P.head_chunk - 1) / P.head_chunk;
   P.max_blocks_per_seq = a.max_blocks_per_seq;
@@ -1377,12 +1577,12 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (tc && a.partition_tokens < 1024 && P.head_chunk <= 4 && wl.max_parts > 1 &&
       P.partition_blocks % (4 * P.pair) == 0) {
     const Geometry g2 = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
-                                 P.pair, 2, P.head_chunk, fp8g);
-    if ((fp8g ? 5 : 3) * (g2.smem_bytes + 1024) <= 228 * 1024) P.ppc = 2;
+                                 P.pair, 2, P.head_chunk, shallow);
+    if ((shallow ? 5 : 3) * (g2.smem_bytes + 1024) <= 228 * 1024) P.ppc = 2;
   }
   P.max_groups = (wl.max_parts + P.ppc - 1) / P.ppc;
   const Geometry g = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
-                              P.pair, P.ppc, P.head_chunk, fp8g);
+                              P.pair, P.ppc, P.head_chunk, shallow);
   P.merge_off = g.merge_off;
   if (g.smem_bytes > kMaxSmem) return PKV_EUNSUPPORTED;
   P.stages = g.stages;
@@ -1409,7 +1609,9 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
                       BS, tc))
     return PKV_ECUDA;
 
-  KernelFn fn = fp8g     ? (a.dtype == PKV_BF16 ? fp8g_kernel_for<__nv_bfloat16>(BS)
+  KernelFn fn = tcg      ? (a.dtype == PKV_BF16 ? tcg_kernel_for<__nv_bfloat16>(BS)
+                                                : tcg_kernel_for<__half>(BS))
+                : fp8g     ? (a.dtype == PKV_BF16 ? fp8g_kernel_for<__nv_bfloat16>(BS)
                                                 : fp8g_kernel_for<__half>(BS))
                 : a.kv_fp8 ? (a.dtype == PKV_BF16 ? fp8_kernel_for<__nv_bfloat16>(BS)
                                                 : fp8_kernel_for<__half>(BS))
