@@ -44,14 +44,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # beside it (profiles/ holds the captures).
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each
-    "13b-mha-b64-bf16@2048": {"bytes": 1408830208 + 3778560, "decode_cu_sha": "319b66ed338144c4"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963482368 + 6345984, "decode_cu_sha": "319b66ed338144c4"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328503040 + 4684544, "decode_cu_sha": "319b66ed338144c4"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4295698688 + 35986432, "decode_cu_sha": "319b66ed338144c4"},
-    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704768512 + 9554176, "decode_cu_sha": "319b66ed338144c4"},
-    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483278592 + 8974336, "decode_cu_sha": "319b66ed338144c4"},
-    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 165059840 + 5685248, "decode_cu_sha": "319b66ed338144c4"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2160471552 + 55312128, "decode_cu_sha": "319b66ed338144c4"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408846848 + 3883264, "decode_cu_sha": "d021bbd79c7e1b6e"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963336192 + 6732032, "decode_cu_sha": "d021bbd79c7e1b6e"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328733952 + 5451008, "decode_cu_sha": "d021bbd79c7e1b6e"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4296127232 + 40430080, "decode_cu_sha": "d021bbd79c7e1b6e"},
+    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704773120 + 9312000, "decode_cu_sha": "d021bbd79c7e1b6e"},
+    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483289088 + 9074688, "decode_cu_sha": "d021bbd79c7e1b6e"},
+    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164988672 + 5345536, "decode_cu_sha": "d021bbd79c7e1b6e"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2160482048 + 55278848, "decode_cu_sha": "d021bbd79c7e1b6e"},
 }
 
 
