@@ -649,7 +649,7 @@ def run_swap(args) -> None:
 
 # DRAM bytes (read + write) per launch of the chunked-prefill kernel on the chunked-prefill
 # batch, from one ncu capture, valid only for the kernel source whose hash is recorded.
-PREFILL_TRAFFIC = {"bytes": 278732800 + 106139392, "prefill_cu_sha": "e46532b8844fa6c1"}
+PREFILL_TRAFFIC = {"bytes": 278737152 + 105802496, "prefill_cu_sha": "9482f7f2d6fada57"}
 
 
 def prefill_traffic() -> float | None:

@@ -213,8 +213,7 @@ int paged_attn_prefill(void* out, const void* q, const void* k_cache, const void
  *
  *   out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, ..., dtype:
  *                as in paged_attn_decode (dtype PKV_BF16 or PKV_F16, head_dim 128,
- *                block_size 16, 32 or 64, a power-of-two number of query heads per KV
- *                head, scale > 0).
+ *                block_size 16, 32 or 64, scale > 0).
  *   group_start  int32 [num_groups + 1], device: group g is the run of sequences
  *                group_start[g] .. group_start[g+1]-1 (non-decreasing, within
  *                [0, num_seqs]); sequences outside every run have no shared prefix.

@@ -21,9 +21,8 @@
 // operand type (row sums of the rounded P).  Keys past a row's limit are masked; value
 // rows past the context (stale slots of the last block) are zeroed in registers.
 //
-// Head size 128 with a power-of-two number of query heads per KV head takes the tcgen05
-// kernel further down (128-row tiles, accumulators in tensor memory); other shapes take
-// the mma.sync kernel.
+// Head size 128 takes the tcgen05 kernel further down (128-row tiles, accumulators in
+// tensor memory); head size 64 takes the mma.sync kernel.
 #include <algorithm>
 #include <climits>
 #include <mutex>
@@ -358,13 +357,15 @@ __global__ void __launch_bounds__(kPrefillThreads)
 }
 
 // ------------------------------------------------------------------------------------------
-// tcgen05 path: head_dim 128, a power-of-two number of query heads per KV head
+// tcgen05 path: head_dim 128
 // ------------------------------------------------------------------------------------------
 //
 // One CTA per (sequence, KV head, 128 packed query rows).  Warps 0-3 run the softmax
-// (thread r owns row r, which is tensor-memory lane r), warp 4 loads the Q tile (one 3-D
-// TMA box per 64 columns) and the 64-token K tiles, warp 6 the V tiles, and warp 5 issues
-// the MMAs from one thread.
+// (thread r owns row r, which is tensor-memory lane r), warp 4 loads the Q tile and the
+// 64-token K tiles, warp 6 the V tiles, and warp 5 issues the MMAs from one thread.
+// With a power-of-two number G of query heads per KV head (at most 128) the Q tile is one
+// 3-D TMA box per 64 columns (G heads x 128/G tokens); with any other G (QT) each softmax
+// thread stages its own query row instead.
 // Tensor memory (256 columns): two 64-column score buffers and the 128-column output.
 //   S_b = Q . K_j^T       (M 128, N 64, K 128; A and B K-major from shared memory)
 //   P_j                   (bf16, written over the first 32 columns of S_b)
@@ -383,7 +384,7 @@ constexpr int kUTile = kUKeys * 128 * 2;   // bytes of a K (or V) tile, head_dim
 constexpr int kUQBytes = kURows * 128 * 2;
 constexpr int kUSmem = 1024 + kUQBytes + kUStages * 2 * kUTile + 256;
 
-template <typename T, int BS>
+template <typename T, int BS, bool QT>
 __global__ void __launch_bounds__(kUThreads, 2)
     prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_base + 1);
 
   if (tid == 0) {
-    mbar_init(smem_addr(q_full), 1);
+    mbar_init(smem_addr(q_full), QT ? 4 : 1);  // QT: one arrival per softmax warp
     for (int i = 0; i < kUStages; ++i) {
       mbar_init(smem_addr(&k_full[i]), 1);
       mbar_init(smem_addr(&k_empty[i]), 1);
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
     const int x0 = g * D;
     if (lane == 0) {
       tma_prefetch_desc(map);
-      if (is_k) {
+      if (is_k && !QT) {
         tma_prefetch_desc(&qmap);
         const uint32_t bar = smem_addr(q_full);
         mbar_arrive_expect_tx(bar, kUQBytes);
@@ -657,6 +658,20 @@ __global__ void __launch_bounds__(kUThreads, 2)
     const int head = g * G + (Rc - i * G);
     const int lim = (P.causal ? L - n + i : ke - 1) - ks;  // last key, relative to ks
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    if constexpr (QT) {
+      // the row's query into the Q tile: two 64-column halves of 128-byte rows, 16-byte
+      // chunk c of row r stored at chunk c ^ (r mod 8) (the 128-byte swizzle the MMA's
+      // shared-memory descriptor describes)
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          static_cast<const T*>(P.q) + (static_cast<size_t>(q0 + i) * P.num_q_heads + head) * D);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(sq + (c >> 3) * (kURows * 128) + r * 128 +
+                                  (((c & 7) ^ (r & 7)) << 4)) = __ldg(qrow + c);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(q_full));
+    }
     float m = -INFINITY, l = 0.f;
     int done = 0;
     for (int j = 0; j < ntiles; ++j) {
@@ -790,7 +805,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
   // wait (bounded) for tile loads still in flight after an abort, then free tensor memory
   if ((tid == 4 * 32 || tid == 6 * 32) && flags[0]) {
     const bool is_k = tid == 4 * 32;
-    if (is_k) mbar_wait_bounded(smem_addr(q_full), 0);
+    if (is_k && !QT) mbar_wait_bounded(smem_addr(q_full), 0);
     uint64_t* fullb = is_k ? k_full : v_full;
     const int issued = flags[is_k ? 1 : 2];
     for (int j = max(0, issued - kUStages); j < issued; ++j)
@@ -804,12 +819,17 @@ __global__ void __launch_bounds__(kUThreads, 2)
 
 using PrefillUmmaFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams);
 
-template <typename T>
-PrefillUmmaFn prefill_umma_for_type(int BS) {
-  if (BS == 16) return prefill_umma_kernel<T, 16>;
-  if (BS == 32) return prefill_umma_kernel<T, 32>;
-  if (BS == 64) return prefill_umma_kernel<T, 64>;
+template <typename T, bool QT>
+PrefillUmmaFn prefill_umma_for(int BS) {
+  if (BS == 16) return prefill_umma_kernel<T, 16, QT>;
+  if (BS == 32) return prefill_umma_kernel<T, 32, QT>;
+  if (BS == 64) return prefill_umma_kernel<T, 64, QT>;
   return nullptr;
+}
+
+template <typename T>
+PrefillUmmaFn prefill_umma_for_type(int BS, bool q_tma) {
+  return q_tma ? prefill_umma_for<T, false>(BS) : prefill_umma_for<T, true>(BS);
 }
 
 using PrefillFn = void (*)(CUtensorMap, CUtensorMap, PrefillParams);
@@ -884,11 +904,10 @@ bool make_q_map(CUtensorMap* map, const void* base, pkv_dtype dt, int T, int Hq,
          CUDA_SUCCESS;
 }
 
-// Whether the tcgen05 kernel serves this shape: head_dim 128 and a power-of-two number of
-// query heads per KV head, at most 128.
-bool umma_path(int head_dim, int group) {
-  return head_dim == 128 && group >= 1 && group <= 128 && (group & (group - 1)) == 0;
-}
+// Whether the tcgen05 kernel serves this shape (head_dim 128), and whether its Q tile is
+// one 3-D TMA box (a power-of-two number of query heads per KV head, at most 128).
+bool umma_path(int head_dim, int group) { return head_dim == 128 && group >= 1; }
+bool umma_q_tma(int group) { return group <= 128 && (group & (group - 1)) == 0; }
 
 constexpr int kMaxPrefillSmem = 227 * 1024;
 
@@ -954,11 +973,13 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
       !make_kv_map(&vmap, a.v_cache, a.dtype, a.num_kv_heads, D, rows, BS))
     return PKV_ECUDA;
   if (umma) {
-    CUtensorMap qmap;
-    if (!make_q_map(&qmap, a.q, a.dtype, a.num_q_tokens, a.num_q_heads, D, P.group))
+    // (with the query rows staged by threads the kernel never reads the Q map)
+    const bool q_tma = umma_q_tma(P.group);
+    CUtensorMap qmap{};
+    if (q_tma && !make_q_map(&qmap, a.q, a.dtype, a.num_q_tokens, a.num_q_heads, D, P.group))
       return PKV_ECUDA;
-    PrefillUmmaFn ufn = a.dtype == PKV_BF16 ? prefill_umma_for_type<__nv_bfloat16>(BS)
-                                            : prefill_umma_for_type<__half>(BS);
+    PrefillUmmaFn ufn = a.dtype == PKV_BF16 ? prefill_umma_for_type<__nv_bfloat16>(BS, q_tma)
+                                            : prefill_umma_for_type<__half>(BS, q_tma);
     if (!ufn) return PKV_EUNSUPPORTED;
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(ufn),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem) != cudaSuccess)

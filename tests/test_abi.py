@@ -106,7 +106,7 @@ def test_argument_checks_return_before_any_cuda_call(lib):
         ctypes.c_int(bs), ctypes.c_int(8), ctypes.c_int(16), ctypes.c_float(scale),
         ctypes.c_int(dt), null, ctypes.c_size_t(0), null)
     assert sp(*spargs(8, 2, 64, 16, 1, 0.1)) == -4     # head_dim 64 not served
-    assert sp(*spargs(12, 4, 128, 16, 1, 0.1)) == -4   # 3 heads per KV head not served
+    assert sp(*spargs(12, 4, 128, 16, 1, 0.1)) == -1   # 3 heads per KV head: served (null ptrs)
     assert sp(*spargs(8, 2, 128, 16, 1, -0.1)) == -4   # negative scale not served
     assert sp(*spargs(8, 2, 128, 16, 1, 0.1)) == -1    # null pointers
     ws = lib.paged_attn_decode_shared_prefix_workspace_size

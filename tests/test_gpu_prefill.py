@@ -55,15 +55,17 @@ PRIOR = [0, 3, 16, 100, 700, 0, 63]
 CHUNK = [1, 17, 64, 5, 130, 70, 65]
 
 SHAPES = [
-    # dtype, Hq, Hkv, D, bs     (head_dim 128 with 1, 2, 4, ... heads per KV head: tcgen05)
+    # dtype, Hq, Hkv, D, bs     (head_dim 128: tcgen05; head_dim 64: mma.sync)
     ("bf16", 4, 4, 128, 16),
     ("bf16", 8, 1, 128, 16),
     ("bf16", 64, 8, 128, 16),
     ("f16", 16, 2, 128, 32),
     ("bf16", 16, 4, 128, 64),
     ("bf16", 32, 2, 128, 16),
-    ("bf16", 12, 4, 128, 16),    # 3 heads per KV head: mma.sync
-    ("bf16", 40, 2, 128, 32),    # 20 heads per KV head: mma.sync
+    ("bf16", 12, 4, 128, 16),    # 3 heads per KV head: a 128-row tile ends inside a token
+    ("bf16", 40, 2, 128, 32),    # 20 heads per KV head
+    ("f16", 30, 5, 128, 16),     # 6 heads per KV head
+    ("bf16", 160, 1, 128, 64),   # 160 heads per KV head: one token spans two tiles
     ("bf16", 12, 4, 64, 64),
     ("bf16", 6, 3, 64, 16),
     ("f16", 2, 2, 64, 32),

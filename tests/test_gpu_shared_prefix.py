@@ -58,7 +58,8 @@ def share_prefix(w, group_start, prefix_lens):
 
 
 @pytest.mark.parametrize("Hq,Hkv,bs,dtype", [(8, 2, 16, "bf16"), (16, 2, 32, "f16"),
-                                             (4, 4, 64, "bf16")])
+                                             (4, 4, 64, "bf16"), (12, 4, 16, "bf16"),
+                                             (10, 2, 32, "f16")])
 def test_groups_of_mixed_sizes_match_oracle(pkv, Hq, Hkv, bs, dtype):
     lens = [200, 70, 64, 900, 33, 40, 1, 300, 64, 0, 17, 500]
     group_start = [0, 4, 5, 9]       # runs [0,4), [4,5), [5,9); 9..11 outside every group
