@@ -44,14 +44,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # beside it (profiles/ holds the captures).
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each
-    "13b-mha-b64-bf16@2048": {"bytes": 1408846848 + 3883264, "decode_cu_sha": "d021bbd79c7e1b6e"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963336192 + 6732032, "decode_cu_sha": "d021bbd79c7e1b6e"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328733952 + 5451008, "decode_cu_sha": "d021bbd79c7e1b6e"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4296127232 + 40430080, "decode_cu_sha": "d021bbd79c7e1b6e"},
-    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704773120 + 9312000, "decode_cu_sha": "d021bbd79c7e1b6e"},
-    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483289088 + 9074688, "decode_cu_sha": "d021bbd79c7e1b6e"},
-    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164988672 + 5345536, "decode_cu_sha": "d021bbd79c7e1b6e"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2160482048 + 55278848, "decode_cu_sha": "d021bbd79c7e1b6e"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408908544 + 3557632, "decode_cu_sha": "c33ade031646219c"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963425536 + 6619904, "decode_cu_sha": "c33ade031646219c"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328653824 + 5491968, "decode_cu_sha": "c33ade031646219c"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4296349440 + 40238592, "decode_cu_sha": "c33ade031646219c"},
+    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704758272 + 3695360, "decode_cu_sha": "c33ade031646219c"},
+    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483133184 + 5581824, "decode_cu_sha": "c33ade031646219c"},
+    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164988160 + 5210624, "decode_cu_sha": "c33ade031646219c"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148133632 + 34915840, "decode_cu_sha": "c33ade031646219c"},
 }
 
 

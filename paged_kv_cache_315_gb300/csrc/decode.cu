@@ -841,7 +841,7 @@ __device__ __forceinline__ void tcg_block(uint32_t kb, uint32_t vb, const uint32
                                           float (&o)[8][4], float (&m)[2], float (&l)[2],
                                           int valid, float scale_log2, int lane) {
   constexpr int MT = BS / 16;
-  const int c = lane & 3, r8 = lane >> 2;
+  const int r8 = lane >> 2;
   float sc[MT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
@@ -1238,7 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 5)
 
 template <typename T>
 KernelFn fp8g_kernel_for(int BS) {
-  if (BS == 16) return decode_fp8g_kernel<T, 16, 2>;
+  if (BS == 16) return decode_fp8g_kernel<T, 16, 1>;  // two 16-token stages per warp
   if (BS == 32) return decode_fp8g_kernel<T, 32, 1>;
   if (BS == 64) return decode_fp8g_kernel<T, 64, 1>;
   return nullptr;
@@ -1570,7 +1570,9 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     P.ws_o = reinterpret_cast<float*>(ws + wl.o_offset);
     P.ws_ml = reinterpret_cast<float*>(ws + wl.ml_offset);
   }
-  P.pair = (a.kv_fp8 && BS == 16) ? 2 : 1;
+  // 16-token E4M3 blocks: the M = heads kernel stacks two per staged tile; the heads-in-N
+  // kernel stages them singly, which gives each warp two stages of the same bytes in flight
+  P.pair = (a.kv_fp8 && BS == 16 && !fp8g) ? 2 : 1;
   // Short partitions on the tensor-core paths: a CTA streams two of them back to back
   // (one partial each) when its merge buffer still lets three CTAs share an SM.
   P.ppc = 1;
