@@ -239,6 +239,37 @@ def traffic_for(w_name: str, part: int, fp8: bool = False) -> float | None:
     return float(entry["bytes"]) if entry.get("decode_cu_sha") == digest else None
 
 
+def decode_kernel_name(w: synth.Workload, fp8: bool) -> str:
+    """The decode kernel the library launches for this batch (the launcher's choice)."""
+    G = w.num_q_heads // w.num_kv_heads
+    if fp8:
+        return "decode_fp8g_kernel" if G <= 8 else "decode_fp8_kernel"
+    if w.dtype not in ("bf16", "f16") or w.head_dim not in (64, 128) or \
+            w.block_size not in (16, 32, 64):
+        return "decode_simt_kernel"
+    return "decode_tcg_kernel" if w.head_dim == 128 and 2 <= G <= 8 else "decode_tc_kernel"
+
+
+def cache_ops(t: dict, w: synth.Workload, fp8: bool, has_pairs: bool, copy_ms: float,
+              write_ms: float) -> dict:
+    """Per-step time and bytes moved (read + write) of the copy-on-write copies and the slot
+    write that precede the decode in every step."""
+    cache_elem = 1 if fp8 else t["k_cache"].element_size()
+    row = w.num_kv_heads * w.head_dim
+    out = {}
+    if has_pairs:
+        pairs = int(t["copy_pairs"].shape[0])
+        nbytes = 2 * pairs * (2 * w.block_size * row * cache_elem + 16)  # K and V calls
+        out["kv_copy_blocks"] = {"calls": 2, "pairs": pairs, "ms": round(copy_ms, 5),
+                                 "bytes": nbytes, "GB/s": round(nbytes / (copy_ms / 1e3) / 1e9, 1)}
+    n = int(t["k_new"].shape[0])
+    nbytes = 2 * n * row * (t["k_new"].element_size() + cache_elem) + 8 * n
+    out["kv_cache_write" + ("_fp8" if fp8 else "")] = {
+        "tokens": n, "ms": round(write_ms, 5), "bytes": nbytes,
+        "GB/s": round(nbytes / (write_ms / 1e3) / 1e9, 1)}
+    return out
+
+
 def max_over_ranks(values, world: int) -> list:
     """Element-wise max of ``values`` over all ranks (the values themselves for one rank)."""
     if world <= 1:
@@ -328,9 +359,15 @@ def run_ours(args) -> None:
             sp_max_group, sp_max_prefix))
 
     def step(inp, ev=None):
+        # ev: events at the step's start, after the copies, after the slot write, after the
+        # decode (the cache ops and the decode are timed separately)
+        if ev is not None:
+            ev[0].record()
         if has_pairs:
             pkv.kv_copy_blocks(t["k_cache"], inp["copy_pairs"])
             pkv.kv_copy_blocks(t["v_cache"], inp["copy_pairs"])
+        if ev is not None:
+            ev[1].record()
         if fp8:
             pkv.kv_cache_write_fp8(inp["k_new"], inp["v_new"], t["k_cache"], t["v_cache"],
                                    inp["slot_mapping"], ks, vs)
@@ -338,7 +375,7 @@ def run_ours(args) -> None:
             pkv.kv_cache_write(inp["k_new"], inp["v_new"], t["k_cache"], t["v_cache"],
                                inp["slot_mapping"])
         if ev is not None:
-            ev[0].record()
+            ev[2].record()
         if cascade:
             pkv.paged_attn_decode_shared_prefix(
                 out, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
@@ -352,7 +389,7 @@ def run_ours(args) -> None:
             pkv.paged_attn_decode(out, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
                                   inp["context_lens"], w.scale, partition_size=part, workspace=ws)
         if ev is not None:
-            ev[1].record()
+            ev[3].record()
 
     # copies (K and V), the slot write, the decode kernel and, when the batch splits contexts
     # (workspace in use), the one-CTA prep kernel before it and the merge kernel after it
@@ -373,7 +410,7 @@ def run_ours(args) -> None:
             dist.barrier()
         torch.cuda.synchronize()
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -386,10 +423,13 @@ def run_ours(args) -> None:
     barrier()
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    copy_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    write_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     if pkv.pkv_device_error() != 0:
         raise RuntimeError("device error bits set during the timed steps")
-    elapsed_ms, decode_ms = max_over_ranks([elapsed_ms, decode_ms], world)
+    elapsed_ms, decode_ms, copy_ms, write_ms = max_over_ranks(
+        [elapsed_ms, decode_ms, copy_ms, write_ms], world)
 
     # end to end: the step's inputs packed in one pinned host buffer, copied in with one
     # transfer, the result read back every step
@@ -470,12 +510,13 @@ def run_ours(args) -> None:
         "queries_per_s": round(B * world / (ms / 1e3), 1),
         "query_heads_per_s": round(B * w.num_q_heads * world / (ms / 1e3), 1),
         "decode_ms": round(decode_ms, 5),
+        "cache_ops": cache_ops(t, w, fp8, has_pairs, copy_ms, write_ms),
         "partition_tokens": part,
         "kv_dtype": "e4m3" if fp8 else w.dtype,
         "roofline": {"kernel": ("paged_attn_decode_shared_prefix (prep, prefix and suffix "
                                 "passes of prefill_umma_kernel, merge)" if cascade else
-                                ("paged_attn_decode_fp8 (decode_fp8_kernel" if fp8
-                                 else "paged_attn_decode (decode_tc_kernel")
+                                ("paged_attn_decode_fp8 (" if fp8 else "paged_attn_decode (")
+                                + decode_kernel_name(w, fp8)
                                 + (" + prep + merge grids)" if split else ")")), "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
