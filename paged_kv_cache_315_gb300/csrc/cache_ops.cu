@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+constexpr int kCopyUnroll = 4;  // vectors a thread moves per group (the grid gives it 4)
+
 // cache block dst <- cache block src for every pair; blockIdx.y strides over pairs.
 template <typename V>
 __global__ void __launch_bounds__(kThreads)
@@ -64,9 +66,17 @@ __global__ void __launch_bounds__(kThreads)
     const V* s = cache + src * vec_per_block;
     V* d = cache + dst * vec_per_block;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-         i < vec_per_block; i += stride)
-      d[i] = s[i];
+    long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    // every load of a group before its stores: destinations never overlap sources (the
+    // call's contract), so a thread keeps kCopyUnroll reads in flight instead of one
+    for (; i + (kCopyUnroll - 1) * stride < vec_per_block; i += kCopyUnroll * stride) {
+      V r[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) r[u] = s[i + u * stride];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) d[i + u * stride] = r[u];
+    }
+    for (; i < vec_per_block; i += stride) d[i] = s[i];
   }
 }
 
