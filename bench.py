@@ -358,9 +358,8 @@ def run_ours(args) -> None:
             B, len(pls), w.num_q_heads, w.num_kv_heads, w.block_size, w.max_blocks_per_seq,
             sp_max_group, sp_max_prefix))
 
-    def step(inp, ev=None):
-        # ev: events at the step's start, after the copies, after the slot write, after the
-        # decode (the cache ops and the decode are timed separately)
+    def cache_step(inp, ev=None):
+        # ev (the separate cache-op timing pass only): start, after the copies, after the write
         if ev is not None:
             ev[0].record()
         if has_pairs:
@@ -376,6 +375,12 @@ def run_ours(args) -> None:
                                inp["slot_mapping"])
         if ev is not None:
             ev[2].record()
+
+    def step(inp, ev=None):
+        # ev: events around the decode call, inside the timed steps
+        cache_step(inp)
+        if ev is not None:
+            ev[0].record()
         if cascade:
             pkv.paged_attn_decode_shared_prefix(
                 out, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
@@ -389,7 +394,7 @@ def run_ours(args) -> None:
             pkv.paged_attn_decode(out, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
                                   inp["context_lens"], w.scale, partition_size=part, workspace=ws)
         if ev is not None:
-            ev[3].record()
+            ev[1].record()
 
     # copies (K and V), the slot write, the decode kernel and, when the batch splits contexts
     # (workspace in use), the one-CTA prep kernel before it and the merge kernel after it
@@ -410,7 +415,7 @@ def run_ours(args) -> None:
             dist.barrier()
         torch.cuda.synchronize()
 
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2))
            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -423,11 +428,21 @@ def run_ours(args) -> None:
     barrier()
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    decode_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    copy_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    write_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    decode_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     if pkv.pkv_device_error() != 0:
         raise RuntimeError("device error bits set during the timed steps")
+    # the cache operations alone, in a pass of their own (events inside the timed steps
+    # would lengthen them)
+    # A busy-wait kernel holds the GPU while the host enqueues the whole pass, so the events
+    # time the kernels, not the host's launch rate.
+    cevs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+            for _ in range(args.steps)]
+    torch.cuda._sleep(int(2e6 + 1e5 * args.steps))
+    for i in range(args.steps):
+        cache_step(t, cevs[i])
+    torch.cuda.synchronize()
+    copy_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in cevs)
+    write_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in cevs)
     elapsed_ms, decode_ms, copy_ms, write_ms = max_over_ranks(
         [elapsed_ms, decode_ms, copy_ms, write_ms], world)
 

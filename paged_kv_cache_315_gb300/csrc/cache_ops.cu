@@ -35,14 +35,15 @@ __global__ void __launch_bounds__(kThreads)
        i += stride) {
     const long long t = i / vec_per_row;
     const long long col = i - t * vec_per_row;
+    // the row loads do not depend on the slot: all three are in flight together
     const long long slot = __ldg(&slots[t]);
+    const V kv = __ldg(&k[i]);
+    const V vv = __ldg(&v[i]);
     if (slot < 0) continue;  // padding
     if (slot >= num_rows) {
       if (col == 0) raise_error(err, PKV_DERR_SLOT);
       continue;
     }
-    const V kv = __ldg(&k[i]);
-    const V vv = __ldg(&v[i]);
     kc[slot * vec_per_row + col] = kv;
     vc[slot * vec_per_row + col] = vv;
   }
@@ -120,7 +121,14 @@ __global__ void __launch_bounds__(kThreads)
        i += stride) {
     const long long t = i / groups;
     const int e0 = static_cast<int>(i - t * groups) * 8;
+    // the row loads do not depend on the slot: all of them are in flight together
     const long long slot = __ldg(&slots[t]);
+    float fk[8], fv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      fk[e] = to_f32(k[t * row_elems + e0 + e]);
+      fv[e] = to_f32(v[t * row_elems + e0 + e]);
+    }
     if (slot < 0) continue;
     if (slot >= num_rows) {
       if (e0 == 0) raise_error(err, PKV_DERR_SLOT);
@@ -129,8 +137,8 @@ __global__ void __launch_bounds__(kThreads)
     uint8_t ck[8], cv[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float xk = __fdiv_rn(to_f32(k[t * row_elems + e0 + e]), k_scale);
-      const float xv = __fdiv_rn(to_f32(v[t * row_elems + e0 + e]), v_scale);
+      const float xk = __fdiv_rn(fk[e], k_scale);
+      const float xv = __fdiv_rn(fv[e], v_scale);
       ck[e] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(xk, __NV_SATFINITE, __NV_E4M3));
       cv[e] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(xv, __NV_SATFINITE, __NV_E4M3));
     }
