@@ -52,6 +52,7 @@ MEASURED_TRAFFIC: dict = {
     "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483133184 + 5581824, "decode_cu_sha": "c33ade031646219c"},
     "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164988160 + 5210624, "decode_cu_sha": "c33ade031646219c"},
     "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148133632 + 34915840, "decode_cu_sha": "c33ade031646219c"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 2102498560, "decode_cu_sha": "c33ade031646219c"},
 }
 
 
@@ -226,6 +227,27 @@ class ClockSampler:
         reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
                 "samples": len(rows), "reasons": reasons}
+
+
+# DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
+# suffix ordering and decode, merge), valid only for the recorded sources
+CASCADE_TRAFFIC: dict = {
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393178112, "sources_sha": "5f8b511026ddc891"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 354241536, "sources_sha": "5f8b511026ddc891"},
+}
+CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
+
+
+def cascade_traffic_for(w_name: str, part: int) -> float | None:
+    import hashlib
+
+    entry = CASCADE_TRAFFIC.get(f"{w_name}@{part}")
+    if not entry:
+        return None
+    h = hashlib.sha256()
+    for f in CASCADE_SOURCES:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_315_gb300", "csrc", f), "rb").read())
+    return float(entry["bytes"]) if entry["sources_sha"] == h.hexdigest()[:16] else None
 
 
 def traffic_for(w_name: str, part: int, fp8: bool = False) -> float | None:
@@ -536,7 +558,8 @@ def run_ours(args) -> None:
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": ab,
-                     "traffic": None if cascade else traffic_for(w.name, part, fp8)},
+                     "traffic": (cascade_traffic_for(w.name, part) if cascade
+                                 else traffic_for(w.name, part, fp8))},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
