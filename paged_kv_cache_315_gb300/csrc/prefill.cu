@@ -384,7 +384,7 @@ constexpr int kUTile = kUKeys * 128 * 2;   // bytes of a K (or V) tile, head_dim
 constexpr int kUQBytes = kURows * 128 * 2;
 constexpr int kUSmem = 1024 + kUQBytes + kUStages * 2 * kUTile + 256;
 
-template <typename T, int BS, bool QT>
+template <typename T, int BS, bool QT, bool WI>
 __global__ void __launch_bounds__(kUThreads, 2)
     prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
@@ -590,13 +590,25 @@ __global__ void __launch_bounds__(kUThreads, 2)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) {
+      const uint32_t vb = smem_addr(vt);
+      if constexpr (WI) {
+        // the whole (converged) warp runs the issue; lane 0 performs it
+        const uint32_t iss = lane == 0;
         tc_fence_after_sync();
-        const uint32_t vb = smem_addr(vt);
 #pragma unroll
         for (int kt = 0; kt < kUKeys / 16; ++kt)
-          umma_ts(tm_o, tm + b * kUKeys + kt * 8, smem_desc_sw128(vb + kt * 2048, kUKeys * 128, 1024),
-                  kIdPV, (i > 0 || kt > 0) ? 1u : 0u);
+          umma_ts_warp(iss, tm_o, tm + b * kUKeys + kt * 8,
+                       smem_desc_sw128(vb + kt * 2048, kUKeys * 128, 1024), kIdPV,
+                       (i > 0 || kt > 0) ? 1u : 0u);
+        umma_commit_warp(iss, smem_addr(&v_empty[st]));
+        umma_commit_warp(iss, smem_addr(pv_done));
+      } else if (lane == 0) {
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kt = 0; kt < kUKeys / 16; ++kt)
+          umma_ts(tm_o, tm + b * kUKeys + kt * 8,
+                  smem_desc_sw128(vb + kt * 2048, kUKeys * 128, 1024), kIdPV,
+                  (i > 0 || kt > 0) ? 1u : 0u);
         umma_commit(smem_addr(&v_empty[st]));
         umma_commit(smem_addr(pv_done));
       }
@@ -625,7 +637,18 @@ __global__ void __launch_bounds__(kUThreads, 2)
         }
       }
       const uint32_t kb = smem_addr(ring + st * 2 * kUTile);
-      if (lane == 0) {
+      if constexpr (WI) {
+        const uint32_t iss = lane == 0;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss_warp(iss, tm + b * kUKeys,
+                       smem_desc_sw128(qb + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(kb + (kk >> 2) * (kUKeys * 128) + (kk & 3) * 32, 16, 1024),
+                       kIdQK, kk > 0 ? 1u : 0u);
+        umma_commit_warp(iss, smem_addr(&k_empty[st]));
+        umma_commit_warp(iss, smem_addr(&s_full[b]));
+      } else if (lane == 0) {
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -819,17 +842,22 @@ __global__ void __launch_bounds__(kUThreads, 2)
 
 using PrefillUmmaFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams);
 
-template <typename T, bool QT>
+template <typename T, bool QT, bool WI>
 PrefillUmmaFn prefill_umma_for(int BS) {
-  if (BS == 16) return prefill_umma_kernel<T, 16, QT>;
-  if (BS == 32) return prefill_umma_kernel<T, 32, QT>;
-  if (BS == 64) return prefill_umma_kernel<T, 64, QT>;
+  if (BS == 16) return prefill_umma_kernel<T, 16, QT, WI>;
+  if (BS == 32) return prefill_umma_kernel<T, 32, QT, WI>;
+  if (BS == 64) return prefill_umma_kernel<T, 64, QT, WI>;
   return nullptr;
 }
 
+// q_tma: the Q tile by TMA (else staged by the softmax threads); warp_issue: MMAs issued by
+// the converged warp (causal chunks) rather than from a lane-0 branch (the options of the
+// shared-prefix passes), the faster form for each on GB300
 template <typename T>
-PrefillUmmaFn prefill_umma_for_type(int BS, bool q_tma) {
-  return q_tma ? prefill_umma_for<T, false>(BS) : prefill_umma_for<T, true>(BS);
+PrefillUmmaFn prefill_umma_for_type(int BS, bool q_tma, bool warp_issue) {
+  if (warp_issue)
+    return q_tma ? prefill_umma_for<T, false, true>(BS) : prefill_umma_for<T, true, true>(BS);
+  return q_tma ? prefill_umma_for<T, false, false>(BS) : prefill_umma_for<T, true, false>(BS);
 }
 
 using PrefillFn = void (*)(CUtensorMap, CUtensorMap, PrefillParams);
@@ -978,8 +1006,10 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     CUtensorMap qmap{};
     if (q_tma && !make_q_map(&qmap, a.q, a.dtype, a.num_q_tokens, a.num_q_heads, D, P.group))
       return PKV_ECUDA;
-    PrefillUmmaFn ufn = a.dtype == PKV_BF16 ? prefill_umma_for_type<__nv_bfloat16>(BS, q_tma)
-                                            : prefill_umma_for_type<__half>(BS, q_tma);
+    const bool warp_issue = !options;
+    PrefillUmmaFn ufn =
+        a.dtype == PKV_BF16 ? prefill_umma_for_type<__nv_bfloat16>(BS, q_tma, warp_issue)
+                            : prefill_umma_for_type<__half>(BS, q_tma, warp_issue);
     if (!ufn) return PKV_EUNSUPPORTED;
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(ufn),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem) != cudaSuccess)
