@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kPrefillThreads)
 }
 
 // ------------------------------------------------------------------------------------------
-// tcgen05 path: head_dim 128
+// tcgen05 path: head_dim 64 or 128
 // ------------------------------------------------------------------------------------------
 //
 // One CTA per (sequence, KV head, 128 packed query rows).  Warps 0-3 run the softmax
@@ -380,17 +380,24 @@ constexpr int kURows = 128;       // packed query rows per CTA
 constexpr int kUKeys = 64;        // key tokens per tile
 constexpr int kUStages = 2;       // K/V ring depth
 constexpr int kUTmemCols = 256;
-constexpr int kUTile = kUKeys * 128 * 2;   // bytes of a K (or V) tile, head_dim 128
-constexpr int kUQBytes = kURows * 128 * 2;
-constexpr int kUSmem = 1024 + kUQBytes + kUStages * 2 * kUTile + 256;
+// bytes of a K (or V) tile, of the Q tile, and the dynamic shared memory, for head_dim D
+// (D / 64 boxes of 64 columns per row, each box 128-byte rows)
+__host__ __device__ constexpr int u_tile(int D) { return kUKeys * D * 2; }
+__host__ __device__ constexpr int u_qbytes(int D) { return kURows * D * 2; }
+__host__ __device__ constexpr int u_smem(int D) {
+  return 1024 + u_qbytes(D) + kUStages * 2 * u_tile(D) + 256;
+}
 
-template <typename T, int BS, bool QT, bool WI>
+template <typename T, int D, int BS, bool QT, bool WI>
 __global__ void __launch_bounds__(kUThreads, 2)
     prefill_umma_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap,
                         const __grid_constant__ CUtensorMap qmap, const PrefillParams P) {
-  constexpr int D = 128;
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   constexpr int NBT = kUKeys / BS;
+  constexpr int NBX = D / 64;                  // 64-column boxes per row
+  constexpr int kUTile = u_tile(D);
+  constexpr int kUQBytes = u_qbytes(D);
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
   constexpr uint32_t kIdQK = umma_idesc(kURows, kUKeys, kBf16, false);
   constexpr uint32_t kIdPV = umma_idesc(kURows, D, kBf16, true);
@@ -513,8 +520,10 @@ __global__ void __launch_bounds__(kUThreads, 2)
         tma_prefetch_desc(&qmap);
         const uint32_t bar = smem_addr(q_full);
         mbar_arrive_expect_tx(bar, kUQBytes);
-        tma_load_3d(smem_addr(sq), &qmap, bar, 0, g * G, q0 + row0 / G);
-        tma_load_3d(smem_addr(sq) + kURows * 128, &qmap, bar, 64, g * G, q0 + row0 / G);
+#pragma unroll
+        for (int b = 0; b < NBX; ++b)
+          tma_load_3d(smem_addr(sq) + b * (kURows * 128), &qmap, bar, 64 * b, g * G,
+                      q0 + row0 / G);
       }
     }
     int issued = 0;
@@ -549,7 +558,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
 #pragma unroll
         for (int k = 0; k < NBT; ++k) {
 #pragma unroll
-          for (int b = 0; b < 2; ++b)
+          for (int b = 0; b < NBX; ++b)
             tma_load_2d(dst + b * (kUKeys * 128) + k * (BS * 128), map, bar, x0 + b * 64, ys[k]);
         }
       }
@@ -582,7 +591,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
       const int vrows = L - ks - i * kUKeys;
       if (vrows < kUKeys) {
         const int nz = (kUKeys - vrows) * 8;  // 16-byte chunks per box
-        for (int e = lane; e < 2 * nz; e += 32) {
+        for (int e = lane; e < NBX * nz; e += 32) {
           const int bx = e / nz, rem = e - bx * nz;
           *reinterpret_cast<uint4*>(vt + bx * (kUKeys * 128) + (vrows + rem / 8) * 128 +
                                     (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
@@ -682,13 +691,13 @@ __global__ void __launch_bounds__(kUThreads, 2)
     const int lim = (P.causal ? L - n + i : ke - 1) - ks;  // last key, relative to ks
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
     if constexpr (QT) {
-      // the row's query into the Q tile: two 64-column halves of 128-byte rows, 16-byte
-      // chunk c of row r stored at chunk c ^ (r mod 8) (the 128-byte swizzle the MMA's
-      // shared-memory descriptor describes)
+      // the row's query into the Q tile: D / 64 boxes of 128-byte rows, 16-byte chunk c of
+      // row r stored at chunk c ^ (r mod 8) (the 128-byte swizzle the MMA's shared-memory
+      // descriptor describes)
       const uint4* qrow = reinterpret_cast<const uint4*>(
           static_cast<const T*>(P.q) + (static_cast<size_t>(q0 + i) * P.num_q_heads + head) * D);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < D / 8; ++c)
         *reinterpret_cast<uint4*>(sq + (c >> 3) * (kURows * 128) + r * 128 +
                                   (((c & 7) ^ (r & 7)) << 4)) = __ldg(qrow + c);
       fence_proxy_async_smem();
@@ -842,22 +851,31 @@ __global__ void __launch_bounds__(kUThreads, 2)
 
 using PrefillUmmaFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, PrefillParams);
 
-template <typename T, bool QT, bool WI>
+template <typename T, int D, bool QT, bool WI>
 PrefillUmmaFn prefill_umma_for(int BS) {
-  if (BS == 16) return prefill_umma_kernel<T, 16, QT, WI>;
-  if (BS == 32) return prefill_umma_kernel<T, 32, QT, WI>;
-  if (BS == 64) return prefill_umma_kernel<T, 64, QT, WI>;
+  if (BS == 16) return prefill_umma_kernel<T, D, 16, QT, WI>;
+  if (BS == 32) return prefill_umma_kernel<T, D, 32, QT, WI>;
+  if (BS == 64) return prefill_umma_kernel<T, D, 64, QT, WI>;
   return nullptr;
 }
 
 // q_tma: the Q tile by TMA (else staged by the softmax threads); warp_issue: MMAs issued by
 // the converged warp (causal chunks) rather than from a lane-0 branch (the options of the
-// shared-prefix passes), the faster form for each on GB300
+// shared-prefix passes), the faster form for each on GB300.  head_dim 64 serves plain chunked
+// prefill only (the shared-prefix passes use head_dim 128).
 template <typename T>
-PrefillUmmaFn prefill_umma_for_type(int BS, bool q_tma, bool warp_issue) {
+PrefillUmmaFn prefill_umma_for_type(int D, int BS, bool q_tma, bool warp_issue) {
+  if (D == 64) {
+    if (!warp_issue) return nullptr;
+    return q_tma ? prefill_umma_for<T, 64, false, true>(BS)
+                 : prefill_umma_for<T, 64, true, true>(BS);
+  }
+  if (D != 128) return nullptr;
   if (warp_issue)
-    return q_tma ? prefill_umma_for<T, false, true>(BS) : prefill_umma_for<T, true, true>(BS);
-  return q_tma ? prefill_umma_for<T, false, false>(BS) : prefill_umma_for<T, true, false>(BS);
+    return q_tma ? prefill_umma_for<T, 128, false, true>(BS)
+                 : prefill_umma_for<T, 128, true, true>(BS);
+  return q_tma ? prefill_umma_for<T, 128, false, false>(BS)
+               : prefill_umma_for<T, 128, true, false>(BS);
 }
 
 using PrefillFn = void (*)(CUtensorMap, CUtensorMap, PrefillParams);
@@ -932,9 +950,12 @@ bool make_q_map(CUtensorMap* map, const void* base, pkv_dtype dt, int T, int Hq,
          CUDA_SUCCESS;
 }
 
-// Whether the tcgen05 kernel serves this shape (head_dim 128), and whether its Q tile is
-// one 3-D TMA box (a power-of-two number of query heads per KV head, at most 128).
-bool umma_path(int head_dim, int group) { return head_dim == 128 && group >= 1; }
+// Whether the tcgen05 kernel serves this shape (head_dim 64 or 128), and whether its Q tile
+// is one 3-D TMA box per 64 columns (a power-of-two number of query heads per KV head, at
+// most 128).
+bool umma_path(int head_dim, int group) {
+  return (head_dim == 64 || head_dim == 128) && group >= 1;
+}
 bool umma_q_tma(int group) { return group <= 128 && (group & (group - 1)) == 0; }
 
 constexpr int kMaxPrefillSmem = 227 * 1024;
@@ -946,10 +967,11 @@ bool prefill_supported(pkv_dtype dtype, int head_dim, int block_size) {
          (block_size == 16 || block_size == 32 || block_size == 64);
 }
 
+// The tcgen05 kernel with the shared-prefix options (partials of 128 columns): head_dim 128.
 bool prefill_umma_supported(pkv_dtype dtype, int head_dim, int block_size, int group,
                             float scale) {
-  return prefill_supported(dtype, head_dim, block_size) && umma_path(head_dim, group) &&
-         scale > 0.f;
+  return prefill_supported(dtype, head_dim, block_size) && head_dim == 128 &&
+         umma_path(head_dim, group) && scale > 0.f;
 }
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
@@ -987,7 +1009,8 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   P.part_ml = a.part_ml;
   P.ksplit = a.ksplit > 0 ? a.ksplit : 1;
   const bool options = a.kv_start || a.table_rows || a.non_causal || a.part_o || P.ksplit > 1;
-  if (options && (!umma || (P.ksplit > 1 && P.causal) || (!a.part_o && P.ksplit > 1)))
+  if (options &&
+      (!umma || D != 128 || (P.ksplit > 1 && P.causal) || (!a.part_o && P.ksplit > 1)))
     return PKV_EUNSUPPORTED;
   const long long grid =
       static_cast<long long>(a.num_seqs) * P.m_tiles * a.num_kv_heads * P.ksplit;
@@ -1008,13 +1031,14 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
       return PKV_ECUDA;
     const bool warp_issue = !options;
     PrefillUmmaFn ufn =
-        a.dtype == PKV_BF16 ? prefill_umma_for_type<__nv_bfloat16>(BS, q_tma, warp_issue)
-                            : prefill_umma_for_type<__half>(BS, q_tma, warp_issue);
+        a.dtype == PKV_BF16 ? prefill_umma_for_type<__nv_bfloat16>(D, BS, q_tma, warp_issue)
+                            : prefill_umma_for_type<__half>(D, BS, q_tma, warp_issue);
     if (!ufn) return PKV_EUNSUPPORTED;
+    const int usmem = u_smem(D);
     if (cudaFuncSetAttribute(reinterpret_cast<const void*>(ufn),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem) != cudaSuccess)
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, usmem) != cudaSuccess)
       return PKV_ECUDA;
-    ufn<<<static_cast<unsigned>(grid), kUThreads, kUSmem, stream>>>(kmap, vmap, qmap, P);
+    ufn<<<static_cast<unsigned>(grid), kUThreads, usmem, stream>>>(kmap, vmap, qmap, P);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ECUDA;
   }
   PrefillFn fn = a.dtype == PKV_BF16 ? prefill_kernel_for_type<__nv_bfloat16>(D, BS)

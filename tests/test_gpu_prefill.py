@@ -55,7 +55,7 @@ PRIOR = [0, 3, 16, 100, 700, 0, 63]
 CHUNK = [1, 17, 64, 5, 130, 70, 65]
 
 SHAPES = [
-    # dtype, Hq, Hkv, D, bs     (head_dim 128: tcgen05; head_dim 64: mma.sync)
+    # dtype, Hq, Hkv, D, bs     (tcgen05 for head_dim 64 and 128)
     ("bf16", 4, 4, 128, 16),
     ("bf16", 8, 1, 128, 16),
     ("bf16", 64, 8, 128, 16),
@@ -82,6 +82,20 @@ def test_prefill_matches_oracle(pkv, dtype, Hq, Hkv, D, bs):
     assert pkv.pkv_device_error() == 0
     assert_close(out.float().cpu().numpy(), oracle_prefill(w),
                  f"{dtype} Hq{Hq} Hkv{Hkv} D{D} bs{bs}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_negative_scale_matches_oracle(pkv, D):
+    # a scale that is not positive takes the mma.sync kernel (the tcgen05 kernel folds a
+    # positive scale into its exponent after taking the maximum of the raw scores)
+    w = synth.make_prefill_workload("pfn", seed=16 + D, dtype="bf16", prior_lens=[0, 40, 130],
+                                    chunk_lens=[17, 64, 9], num_q_heads=8, num_kv_heads=2,
+                                    head_dim=D, block_size=16)
+    w.scale = -w.scale
+    t = synth.to_torch(w, "cuda")
+    out = gpu_prefill(pkv, w, t)
+    assert pkv.pkv_device_error() == 0
+    assert_close(out.float().cpu().numpy(), oracle_prefill(w), f"negative scale D{D}")
 
 
 def test_prefill_of_one_token_chunks_matches_decode_oracle(pkv):
