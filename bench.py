@@ -232,8 +232,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393168640, "sources_sha": "88cda6164bc56577"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 354200320, "sources_sha": "88cda6164bc56577"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393096448, "sources_sha": "ec44e244c4cbafe9"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 354257408, "sources_sha": "ec44e244c4cbafe9"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 
@@ -769,7 +769,7 @@ def run_swap(args) -> None:
 
 # DRAM bytes (read + write) per launch of the chunked-prefill kernel on the chunked-prefill
 # batch, from one ncu capture, valid only for the kernel source whose hash is recorded.
-PREFILL_TRAFFIC = {"bytes": 278720256 + 105863168, "prefill_cu_sha": "59bde66e6051515b"}
+PREFILL_TRAFFIC = {"bytes": 278724608 + 106193664, "prefill_cu_sha": "4d7a49772f687c7e"}
 
 
 def prefill_traffic() -> float | None:
