@@ -611,6 +611,31 @@ def test_prefill_matches_causal_sdpa_on_unpaged_sequence(oracle_mod, dtype, Hq, 
                                    atol=1e-13)
 
 
+def test_prefill_with_a_negative_scale_matches_sdpa(oracle_mod):
+    """A negative scale (the GPU tests use one to reach the mma.sync prefill kernel): the
+    rows still equal causal SDPA with that scale, here with 3 query heads per KV head.
+    Catches: a scale sign dropped or taken as its magnitude, a GQA map that assumes a
+    power-of-two group."""
+    w = _pf(dtype="bf16", prior=(0, 9, 40), chunk=(5, 16, 3), Hq=9, Hkv=3, D=64, bs=16,
+            shuffle=False, scale=-0.21)
+    out = _run_pf(oracle_mod, w)
+    G = w.num_q_heads // w.num_kv_heads
+    q = _f64(w, w.chunk_q)
+    for s in range(w.num_seqs):
+        k, v = _dense_rows(w, s)
+        L = int(w.context_lens[s])
+        a, b = int(w.query_start[s]), int(w.query_start[s + 1])
+        n = b - a
+        kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qt = torch.from_numpy(q[a:b]).permute(1, 0, 2)
+        mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
+                                                               scale=w.scale)
+        np.testing.assert_allclose(out[a:b], ref.permute(1, 0, 2).numpy(), rtol=1e-12,
+                                   atol=1e-13)
+
+
 def test_prefill_row_equals_decode_of_truncated_context(oracle_mod):
     """Row i of a chunk is a decode query over the first L - n + i + 1 tokens.
 
