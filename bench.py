@@ -72,6 +72,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--kv-dtype", choices=["same", "fp8"], default="same",
                    help="cache element type: the batch's own (default) or fp8 E4M3 codes")
+    p.add_argument("--head-dim", type=int, default=128, choices=[64, 128],
+                   help="head_dim of the chunked-prefill batch (--op prefill)")
     p.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
                    help="decode (default): the decode step; swap: block swaps device <-> host; "
                         "prefill: chunked-prefill attention")
@@ -769,12 +771,17 @@ def run_swap(args) -> None:
 
 # DRAM bytes (read + write) per launch of the chunked-prefill kernel on the chunked-prefill
 # batch, from one ncu capture, valid only for the kernel source whose hash is recorded.
-PREFILL_TRAFFIC = {"bytes": 278724608 + 106193664, "prefill_cu_sha": "4d7a49772f687c7e"}
+PREFILL_TRAFFIC = {"workload": "chunked-prefill-70b-gqa8-c512", "bytes": 278724608 + 106193664,
+                   "prefill_cu_sha": "4d7a49772f687c7e"}
 
 
-def prefill_traffic() -> float | None:
+def prefill_traffic(w_name: str) -> float | None:
+    """Recorded DRAM bytes of the benchmark prefill batch (head_dim 128) for the recorded
+    prefill.cu, else None."""
     import hashlib
 
+    if w_name != PREFILL_TRAFFIC["workload"]:
+        return None
     src = os.path.join(ROOT, "paged_kv_cache_315_gb300", "csrc", "prefill.cu")
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     return float(PREFILL_TRAFFIC["bytes"]) if PREFILL_TRAFFIC["prefill_cu_sha"] == digest else None
@@ -814,7 +821,10 @@ def _oracle_prefill_seq(w, s):
 def prefill_config(w) -> dict:
     n = np.diff(w.query_start)
     prior = w.context_lens - n
-    return {"workload": w.name, "recipe": synth.PREFILL_RECIPE, "sequences": w.num_seqs,
+    recipe = synth.PREFILL_RECIPE
+    if w.head_dim != 128:
+        recipe = recipe.replace("head_dim 128", f"head_dim {w.head_dim}")
+    return {"workload": w.name, "recipe": recipe, "sequences": w.num_seqs,
             "chunk_tokens": int(n.max()), "prior_min_mean_max": [int(prior.min()),
                                                                  float(prior.mean()),
                                                                  int(prior.max())],
@@ -829,7 +839,7 @@ def run_prefill(args) -> None:
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    w = synth.prefill_workload()
+    w = synth.prefill_workload(head_dim=args.head_dim)
     if args.impl == "reference":
         if rank != 0:
             return
@@ -963,7 +973,7 @@ def run_prefill(args) -> None:
         "roofline": {"kernel": "paged_attn_prefill (prefill_umma_kernel)", "bound": "tensor",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} bf16_tflops",
-                     "algorithmic_flops_per_launch": flops, "traffic": prefill_traffic(),
+                     "algorithmic_flops_per_launch": flops, "traffic": prefill_traffic(w.name),
                      "traffic_unit": "DRAM bytes per launch"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clk,
     }

@@ -304,13 +304,15 @@ PREFILL_RECIPE = ("chunked prefill bf16: 16 sequences, a 512-token chunk each af
 
 
 def prefill_workload(*, seed: int = BASE_SEED + 6, num_seqs: int = 16, chunk: int = 512,
-                     max_prior: int = 3584) -> Workload:
-    """The chunked-prefill batch (seeded)."""
+                     max_prior: int = 3584, head_dim: int = 128) -> Workload:
+    """The chunked-prefill batch (seeded); ``head_dim`` 64 gives the same batch with
+    64-wide heads."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7])))
     prior = rng.integers(0, max_prior, size=num_seqs, endpoint=True)
-    return make_prefill_workload("chunked-prefill-70b-gqa8-c512", seed=seed, dtype="bf16",
+    name = "chunked-prefill-70b-gqa8-c512" + ("" if head_dim == 128 else f"-d{head_dim}")
+    return make_prefill_workload(name, seed=seed, dtype="bf16",
                                  prior_lens=prior, chunk_lens=[chunk] * num_seqs, num_q_heads=64,
-                                 num_kv_heads=8, head_dim=128, block_size=16,
+                                 num_kv_heads=8, head_dim=head_dim, block_size=16,
                                  max_blocks_per_seq=(max_prior + chunk + 15) // 16)
 
 
