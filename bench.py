@@ -7,8 +7,13 @@ decode attention (split partitions merged by log-sum-exp in the same launch).  T
 pool is device-resident state, as in a serving engine; each step's per-step inputs are
 the query, block tables, context lengths and the new tokens.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
     python bench.py --impl reference ...      # the fp64 CPU oracle on the host cores
+
+By default one process times the decode batches 2 (13B-like MHA), 3 (70B-like GQA with
+slot writes), 4 (shared prefix with copy-on-write) and 5 (32k long context) back to back;
+the line's value is batch 5's and the others are under ``per_config``.  ``--config C``
+times batch C alone.
 
 Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are independent replicas: each
 rank runs the full batch and the value is the sum of all ranks' bytes over the slowest
@@ -61,8 +66,10 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
-    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
-                   help="decode batch (default 2: 13B-like MHA, batch 64)")
+    p.add_argument("--config", type=int, default=0, choices=[0, 1, 2, 3, 4, 5],
+                   help="decode batch; 0 (default): batches 2, 3, 4 and 5 back to back in one "
+                        "process, the 32k long-context batch (5) as the headline and the "
+                        "others under per_config")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--partition", type=int, default=-1,
                    help="partition size in tokens (-1: the batch's own, 0: library default)")
@@ -70,6 +77,9 @@ def parse_args(argv=None):
                    help="CPU time budget of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--flush-l2", action="store_true",
+                   help="also time the decode calls with a 2 x L2 scratch write before each "
+                        "(reported under l2_flushed)")
     p.add_argument("--kv-dtype", choices=["same", "fp8"], default="same",
                    help="cache element type: the batch's own (default) or fp8 E4M3 codes")
     p.add_argument("--head-dim", type=int, default=128, choices=[64, 128],
@@ -386,57 +396,52 @@ def replica_gbs(bytes_per_step: int, steps: int, world: int, seconds: float) -> 
 # our arm
 # ------------------------------------------------------------------------------------------
 
-def run_ours(args) -> None:
+DECODE_CONFIGS = (2, 3, 4, 5)   # the batches one default run times, the last one the headline
+NOMINAL_HBM_GBS = 7900.0        # GB300 HBM3e, nominal (published figure, not measured here)
+
+
+def decode_session(args, cfg: int, dev, pkv):
+    """Device state and step functions of one decode batch (``cfg``, or the grouped-prompt
+    batch with ``--grouped-prefix``)."""
     import torch
-    import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
-    import paged_kv_cache_315_gb300 as pkv
-
-    pkv.load()
-    cfg = args.config
     if args.grouped_prefix:
         w = synth.grouped_prefix_workload()
         synth.add_new_tokens(w, seed=synth.BASE_SEED + 107)
     else:
         w = bench_workload(cfg)
-    part = w.partition_size if args.partition < 0 else args.partition
     t = synth.to_torch(w, dev)
     fp8 = args.kv_dtype == "fp8"
+    ks, vs = fp8_scales(cfg)
     if fp8:
-        ks, vs = fp8_scales(cfg)
         k8, v8 = synth.fp8_kv(w, ks, vs)
         t["k_cache"] = torch.from_numpy(k8).to(dev)
         t["v_cache"] = torch.from_numpy(v8).to(dev)
         del k8, v8
-    step_kv_bytes = kv_bytes(w, fp8)
-    if cfg == 4:
+    if cfg == 4 and not args.grouped_prefix:
         # state: copy-on-write copies, then every suffix token
         pkv.kv_copy_blocks(t["k_cache"], t["copy_pairs"])
         pkv.kv_copy_blocks(t["v_cache"], t["copy_pairs"])
         sk = synth.storage_to_torch(w.info["setup_k"], "bf16", dev)
         sv = synth.storage_to_torch(w.info["setup_v"], "bf16", dev)
         ss = torch.from_numpy(w.info["setup_slots"]).to(dev)
-        if args.kv_dtype == "fp8":
-            pkv.kv_cache_write_fp8(sk, sv, t["k_cache"], t["v_cache"], ss, *fp8_scales(cfg))
+        if fp8:
+            pkv.kv_cache_write_fp8(sk, sv, t["k_cache"], t["v_cache"], ss, ks, vs)
         else:
             pkv.kv_cache_write(sk, sv, t["k_cache"], t["v_cache"], ss)
+        del sk, sv, ss
     out = torch.empty_like(t["q"])
     B = w.num_seqs
+    part = w.partition_size if args.partition < 0 else args.partition
     part = pkv.paged_attn_decode_partition_tokens(B, w.num_q_heads, w.num_kv_heads, w.block_size,
                                                   w.max_blocks_per_seq, part)
-    ws = pkv.workspace_for(dev, pkv.paged_attn_decode_workspace_size(
-        B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.max_blocks_per_seq, part))
+    ws_bytes = pkv.paged_attn_decode_workspace_size(
+        B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.max_blocks_per_seq, part)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     has_pairs = "copy_pairs" in t
 
     cascade = bool(args.shared_prefix)
+    sp = {}
     if cascade:
         if "shared_prefix_tokens" not in w.info or fp8:
             raise SystemExit("--shared-prefix applies to the shared-prefix batches (--config 4, "
@@ -445,11 +450,12 @@ def run_ours(args) -> None:
         pls = w.info.get("prefix_lens", np.array([w.info["shared_prefix_tokens"]], np.int32))
         t["group_start"] = torch.from_numpy(np.ascontiguousarray(gs, np.int32)).to(dev)
         t["prefix_lens"] = torch.from_numpy(np.ascontiguousarray(pls, np.int32)).to(dev)
-        sp_max_group = int(np.diff(gs).max())
-        sp_max_prefix = int(pls.max())
-        sp_ws = pkv.workspace_for(dev, pkv.paged_attn_decode_shared_prefix_workspace_size(
+        sp["max_group"] = int(np.diff(gs).max())
+        sp["max_prefix"] = int(pls.max())
+        nb = pkv.paged_attn_decode_shared_prefix_workspace_size(
             B, len(pls), w.num_q_heads, w.num_kv_heads, w.block_size, w.max_blocks_per_seq,
-            sp_max_group, sp_max_prefix))
+            sp["max_group"], sp["max_prefix"])
+        sp["ws"] = torch.empty(nb, dtype=torch.uint8, device=dev) if nb else None
 
     def cache_step(inp, ev=None):
         # ev (the separate cache-op timing pass only): start, after the copies, after the write
@@ -479,8 +485,8 @@ def run_ours(args) -> None:
         if cascade:
             pkv.paged_attn_decode_shared_prefix(
                 o, inp["q"], t["k_cache"], t["v_cache"], inp["block_tables"],
-                inp["context_lens"], t["group_start"], t["prefix_lens"], sp_max_group,
-                sp_max_prefix, w.scale, workspace=sp_ws)
+                inp["context_lens"], t["group_start"], t["prefix_lens"], sp["max_group"],
+                sp["max_prefix"], w.scale, workspace=sp["ws"])
         elif fp8:
             pkv.paged_attn_decode_fp8(o, inp["q"], t["k_cache"], t["v_cache"],
                                       inp["block_tables"], inp["context_lens"], w.scale, ks, vs,
@@ -494,26 +500,34 @@ def run_ours(args) -> None:
     # copies (K and V), the slot write, the decode kernel and, when the batch splits contexts
     # (workspace in use), the one-CTA prep kernel before it and the merge kernel after it
     # (the batches here stay far below the prep kernel's 65536-item limit)
-    split = ws is not None and ws.numel() > 0
-    launches_per_step = (2 if has_pairs else 0) + 1 + 1 + (2 if split else 0)
+    split = ws is not None
+    launches = (2 if has_pairs else 0) + 1 + 1 + (2 if split else 0)
     if cascade:  # prep, prefix pass, suffix ordering + decode, merge
-        launches_per_step = (2 if has_pairs else 0) + 1 + 5
+        launches = (2 if has_pairs else 0) + 1 + 5
+    names = ["q", "block_tables", "context_lens", "k_new", "v_new", "slot_mapping"]
+    if has_pairs:
+        names.append("copy_pairs")
+    return dict(w=w, t=t, cfg=cfg, fp8=fp8, cascade=cascade, part=part, split=split, out=out,
+                step=step, cache_step=cache_step, has_pairs=has_pairs,
+                launches_per_step=launches, e2e_names=names)
+
+
+def time_decode(args, S, dev, world, barrier, pkv) -> dict:
+    """Warm-up, then K timed steps (whole-step events and per-call decode events), the cache
+    operations in a pass of their own, and the end-to-end pass.  Times are max over ranks."""
+    import torch
+
+    step, t = S["step"], S["t"]
     assert pkv.pkv_device_error() == 0
-    for _ in range(args.warmup):
+    for _ in range(max(3, args.warmup)):
         step(t)
     torch.cuda.synchronize()
     if pkv.pkv_device_error() != 0:
         raise RuntimeError("device error bits set during warm-up")
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-
     evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2))
            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index or 0)
     clocks.start()
     barrier()
     t0.record()
@@ -523,91 +537,199 @@ def run_ours(args) -> None:
     barrier()
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    decode_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    per_call = [e[0].elapsed_time(e[1]) for e in evs]
     if pkv.pkv_device_error() != 0:
         raise RuntimeError("device error bits set during the timed steps")
     # the cache operations alone, in a pass of their own (events inside the timed steps
-    # would lengthen them)
-    # A busy-wait kernel holds the GPU while the host enqueues the whole pass, so the events
-    # time the kernels, not the host's launch rate.
+    # would lengthen them).  A busy-wait kernel holds the GPU while the host enqueues the
+    # whole pass, so the events time the kernels, not the host's launch rate.
     cevs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
             for _ in range(args.steps)]
     torch.cuda._sleep(int(2e6 + 1e5 * args.steps))
     for i in range(args.steps):
-        cache_step(t, cevs[i])
+        S["cache_step"](t, cevs[i])
     torch.cuda.synchronize()
     copy_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in cevs)
     write_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in cevs)
-    elapsed_ms, decode_ms, copy_ms, write_ms = max_over_ranks(
-        [elapsed_ms, decode_ms, copy_ms, write_ms], world)
 
-    # end to end: the step's inputs packed in one pinned host buffer, copied in with one
-    # transfer that overlaps the previous step, the result read back every step
-    e2e = None
+    flushed = None
+    if args.flush_l2:
+        # decode calls with the L2 overwritten before each: a 2 x L2 scratch write on the
+        # same stream between the steps, outside the decode call's events
+        scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+        fevs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2))
+                for _ in range(args.steps)]
+        for i in range(args.steps):
+            scratch.fill_(i & 0xFF)
+            step(t, fevs[i])
+        torch.cuda.synchronize()
+        flushed = statistics.median(a.elapsed_time(b) for a, b in fevs)
+        del scratch
+
+    vals = [elapsed_ms, statistics.mean(per_call), statistics.median(per_call), copy_ms,
+            write_ms, flushed if flushed is not None else 0.0]
+    vals = max_over_ranks(vals, world)
+    r = dict(elapsed_ms=vals[0], decode_ms=vals[1], decode_ms_median=vals[2], copy_ms=vals[3],
+             write_ms=vals[4], decode_ms_l2_flushed=vals[5] if flushed is not None else None,
+             clocks=clk)
+    r["e2e"] = None
     if not args.no_e2e:
-        names = ["q", "block_tables", "context_lens", "k_new", "v_new", "slot_mapping"]
-        if has_pairs:
-            names.append("copy_pairs")
-        e2e_s, h2d, d2h = pipelined_e2e(t, names, out, step, dev, args.steps, args.warmup,
-                                        barrier)
+        e2e_s, h2d, d2h = pipelined_e2e(t, S["e2e_names"], S["out"], step, dev, args.steps,
+                                        args.warmup, barrier)
         (e2e_s,) = max_over_ranks([e2e_s], world)
-        e2e = {"value": round(replica_gbs(step_kv_bytes, args.steps, world, e2e_s), 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e2e_s * 1e3 / args.steps, 4),
-               "path": "per-step inputs packed in one pinned host buffer -> one cudaMemcpyAsync "
-                       "on a copy stream (overlapping the previous step) -> C-ABI calls -> output "
-                       "to pinned host, each step's output waited for one step later"}
+        r["e2e"] = (e2e_s, h2d, d2h)
+    return r
 
+
+def decode_record(args, S, r, world: int) -> dict:
+    """The JSON fields of one timed decode batch."""
+    w, fp8, cascade, part = S["w"], S["fp8"], S["cascade"], S["part"]
+    peak, peak_kind = hbm_peak()
+    ab = algorithmic_bytes(w, fp8)
+    step_kv = kv_bytes(w, fp8)
+    ms = r["elapsed_ms"] / args.steps
+    value = replica_gbs(step_kv, args.steps, world, r["elapsed_ms"] / 1e3)
+    achieved = ab["total"] / (r["decode_ms"] / 1e3) / 1e9
+    traffic = (cascade_traffic_for(w.name, part) if cascade else traffic_for(w.name, part, fp8))
+    if cascade:
+        kernel = ("paged_attn_decode_shared_prefix (prep, prefix and suffix passes of "
+                  "prefill_umma_kernel, merge)")
+    else:
+        kernel = (("paged_attn_decode_fp8 (" if fp8 else "paged_attn_decode (")
+                  + decode_kernel_name(w, fp8) + (" + prep + merge grids)" if S["split"] else ")"))
+    roof = {"kernel": kernel, "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "nominal_peak": NOMINAL_HBM_GBS,
+            "nominal_source": "GB300 HBM3e nominal 7.9 TB/s (published)",
+            "achieved_median": round(ab["total"] / (r["decode_ms_median"] / 1e3) / 1e9, 2),
+            "frac_median": round(ab["total"] / (r["decode_ms_median"] / 1e3) / 1e9 / peak, 4),
+            "algorithmic_bytes_per_launch": ab, "traffic": traffic}
+    rec = {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+        "hbm_frac": round(value / peak, 4),
+        "queries_per_s": round(w.num_seqs * world / (ms / 1e3), 1),
+        "query_heads_per_s": round(w.num_seqs * w.num_q_heads * world / (ms / 1e3), 1),
+        "decode_ms": round(r["decode_ms"], 5), "decode_ms_median": round(r["decode_ms_median"], 5),
+        "partition_tokens": part, "kv_dtype": "e4m3" if fp8 else w.dtype,
+        "cache_ops": cache_ops(S["t"], w, fp8, S["has_pairs"], r["copy_ms"], r["write_ms"]),
+        "roofline": roof, "gpu_launches": S["launches_per_step"] * args.steps,
+        "clocks": r["clocks"],
+    }
+    if "unique_kv_bytes" in describe(w, S["cfg"], part):
+        # logical bytes (what the metric names) count the shared prefix once per sequence;
+        # the fractions below count what HBM must deliver at least (unique rows) and what
+        # it delivered (ncu DRAM bytes of one call, when recorded for this source)
+        ub = unique_kv_bytes(w) // (w.elem_bytes if fp8 else 1)
+        uniq = ub + ab["total"] - ab["kv"]
+        roof["bytes_basis"] = "logical (each sequence's context counted in full)"
+        roof["unique_bytes_per_launch"] = uniq
+        roof["frac_unique_bytes"] = round(uniq / (r["decode_ms"] / 1e3) / 1e9 / peak, 4)
+        roof["frac_dram_bytes"] = (round(traffic / (r["decode_ms"] / 1e3) / 1e9 / peak, 4)
+                                   if traffic else None)
+    if r["decode_ms_l2_flushed"] is not None:
+        rec["l2_flushed"] = {
+            "decode_ms_median": round(r["decode_ms_l2_flushed"], 5),
+            "frac": round(ab["total"] / (r["decode_ms_l2_flushed"] / 1e3) / 1e9 / peak, 4),
+            "how": "2 x L2 scratch written on the stream before every decode call"}
+    if r["e2e"] is not None:
+        e2e_s, h2d, d2h = r["e2e"]
+        rec["e2e"] = {"value": round(replica_gbs(step_kv, args.steps, world, e2e_s), 2),
+                      "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                      "d2h_bytes_per_step": int(d2h),
+                      "ms_per_step": round(e2e_s * 1e3 / args.steps, 4),
+                      "path": "per-step inputs packed in one pinned host buffer -> one "
+                              "cudaMemcpyAsync on a copy stream (overlapping the previous "
+                              "step) -> C-ABI calls -> output to pinned host, each step's "
+                              "output waited for one step later"}
+    else:
+        rec["e2e"] = None
+    return rec
+
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import paged_kv_cache_315_gb300 as pkv
+
+    pkv.load()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    if args.grouped_prefix:
+        cfgs = [0]
+    else:
+        cfgs = list(DECODE_CONFIGS) if args.config == 0 else [args.config]
+    recs, sessions = {}, {}
+    for cfg in cfgs:
+        S = decode_session(args, cfg, dev, pkv)
+        r = time_decode(args, S, dev, world, barrier, pkv)
+        rec = decode_record(args, S, r, world)
+        rec["config"] = dict(describe(S["w"], cfg, S["part"]),
+                             **({"decode": "shared-prefix cascade"} if S["cascade"] else {}))
+        recs[cfg] = rec
+        sessions[cfg] = S["w"]
+        del S
+        torch.cuda.empty_cache()
+
+    head_cfg = cfgs[-1]
+    head = recs[head_cfg]
+    w = sessions[head_cfg]
+    fp8 = args.kv_dtype == "fp8"
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds, fp8_scales(cfg) if fp8 else None)
-
+        cpu = cpu_baseline(w, args.cpu_seconds, fp8_scales(head_cfg) if fp8 else None)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
-    peak, peak_kind = hbm_peak()
-    ab = algorithmic_bytes(w, fp8)
-    ms = elapsed_ms / args.steps
-    value = replica_gbs(step_kv_bytes, args.steps, world, elapsed_ms / 1e3)
-    achieved = ab["total"] / (decode_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": head["value"],
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms, 5),
+        "ms_per_step": head["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": w.dtype if not fp8 else f"{w.dtype} (E4M3 KV cache)",
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
-        "config": dict(describe(w, cfg, part),
-                       **({"decode": "shared-prefix cascade"} if cascade else {})),
-        "hbm_frac": round(value / peak, 4),
-        "queries_per_s": round(B * world / (ms / 1e3), 1),
-        "query_heads_per_s": round(B * w.num_q_heads * world / (ms / 1e3), 1),
-        "decode_ms": round(decode_ms, 5),
-        "cache_ops": cache_ops(t, w, fp8, has_pairs, copy_ms, write_ms),
-        "partition_tokens": part,
-        "kv_dtype": "e4m3" if fp8 else w.dtype,
-        "roofline": {"kernel": ("paged_attn_decode_shared_prefix (prep, prefix and suffix "
-                                "passes of prefill_umma_kernel, merge)" if cascade else
-                                ("paged_attn_decode_fp8 (" if fp8 else "paged_attn_decode (")
-                                + decode_kernel_name(w, fp8)
-                                + (" + prep + merge grids)" if split else ")")), "bound": "hbm",
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                     "algorithmic_bytes_per_launch": ab,
-                     "traffic": (cascade_traffic_for(w.name, part) if cascade
-                                 else traffic_for(w.name, part, fp8))},
-        "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
+        "config": head["config"],
     }
+    for k in ("hbm_frac", "queries_per_s", "query_heads_per_s", "decode_ms", "decode_ms_median",
+              "cache_ops", "partition_tokens", "kv_dtype", "roofline"):
+        line[k] = head[k]
+    if "l2_flushed" in head:
+        line["l2_flushed"] = head["l2_flushed"]
+    line["cpu_baseline"] = cpu
+    line["e2e"] = head["e2e"]
+    line["gpu_launches"] = head["gpu_launches"]
+    line["clocks"] = head["clocks"]
+    if len(cfgs) > 1:
+        line["per_config"] = {}
+        for cfg in cfgs[:-1]:
+            rec = dict(recs[cfg])
+            rec["workload"] = rec["config"]["workload"]
+            line["per_config"][f"config{cfg}"] = rec
+        line["per_config_note"] = (
+            "the other decode batches, timed in the same process before the headline batch "
+            "with the same steps and warm-up; each entry's gpu_launches counts its own timed "
+            "steps")
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -617,43 +739,82 @@ def run_ours(args) -> None:
 # the oracle on the host cores (CPU baseline and reference arm)
 # ------------------------------------------------------------------------------------------
 
-def _oracle_seq(w, s, fp8=None):
+def _oracle_seq(w, s, fp8=None, threads: int = 0):
     import oracle
 
     if fp8 is not None:
         k8, v8, ks, vs = fp8
         return oracle.paged_decode_fp8kv(w.q[s:s + 1], k8, v8, w.block_tables[s:s + 1],
-                                         w.context_lens[s:s + 1], w.scale, ks, vs, w.dtype)
+                                         w.context_lens[s:s + 1], w.scale, ks, vs, w.dtype,
+                                         num_threads=threads)
     return oracle.paged_decode(w.q[s:s + 1], w.k_cache, w.v_cache, w.block_tables[s:s + 1],
-                               w.context_lens[s:s + 1], w.scale, w.dtype)
+                               w.context_lens[s:s + 1], w.scale, w.dtype, num_threads=threads)
 
 
 def seq_kv_bytes(w, s) -> int:
     return int(w.context_lens[s]) * 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
 
 
+def host_cpu() -> dict:
+    """The host's CPU model and core counts."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except Exception:
+        usable = os.cpu_count()
+    return {"model": model, "os_cpu_count": os.cpu_count(), "usable_cores": usable}
+
+
+def _oracle_rate(w, seconds: float, fp8, threads: int) -> tuple[float, int, float]:
+    """GB/s of the oracle over sequences of the batch (cycling) until ``seconds`` pass."""
+    done_bytes, done_seqs = 0, 0
+    s0 = time.perf_counter()
+    while True:
+        s = done_seqs % w.num_seqs
+        _oracle_seq(w, s, fp8, threads)
+        done_bytes += seq_kv_bytes(w, s) // (w.elem_bytes if fp8 else 1)
+        done_seqs += 1
+        el = time.perf_counter() - s0
+        if el >= seconds or done_seqs >= 4 * w.num_seqs:
+            break
+    return done_bytes / el / 1e9, done_seqs, el
+
+
 def cpu_baseline(w, seconds: float, fp8_scale_pair=None) -> dict:
-    """The fp64 oracle, as it stands, over sequences of the batch until ``seconds`` pass."""
+    """The fp64 oracle, as it stands, over sequences of the batch: once on one thread and
+    once with OpenMP over every usable core, ``seconds`` each."""
     import oracle
 
     oracle.build()
     fp8 = None
     if fp8_scale_pair is not None:
         fp8 = (*synth.fp8_kv(w, *fp8_scale_pair), *fp8_scale_pair)
-    done_bytes, done_seqs = 0, 0
-    s0 = time.perf_counter()
-    while True:
-        s = done_seqs % w.num_seqs
-        _oracle_seq(w, s, fp8)
-        done_bytes += seq_kv_bytes(w, s) // (w.elem_bytes if fp8 else 1)
-        done_seqs += 1
-        el = time.perf_counter() - s0
-        if el >= seconds or done_seqs >= 4 * w.num_seqs:
-            break
-    return {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
-            "kind": "oracle",
-            "sample": f"{done_seqs} sequences of the batch (all query heads each) in {el:.1f} s; "
-                      f"fp64 C oracle, OpenMP over (sequence, query head)"}
+    cpu = host_cpu()
+    cores = cpu["usable_cores"]
+    v1, n1, e1 = _oracle_rate(w, seconds / 2, fp8, 1)
+    vn, nn, en = _oracle_rate(w, seconds, fp8, cores)
+    return {"value": round(vn, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nn} sequences of the batch (all query heads each) in {en:.1f} s on "
+                      f"{cores} threads; fp64 C oracle, OpenMP over (sequence, query head)",
+            "single_thread": {"value": round(v1, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{n1} sequences in {e1:.1f} s on one thread"},
+            "cpu": cpu}
 
 
 def run_reference(args) -> None:
@@ -663,20 +824,22 @@ def run_reference(args) -> None:
     import oracle
 
     oracle.build()
-    w = bench_workload(args.config)
+    cfg = args.config or DECODE_CONFIGS[-1]
+    w = bench_workload(cfg)
     part = w.partition_size if args.partition < 0 else args.partition
+    cpu = host_cpu()
+    cores = cpu["usable_cores"]
     order = list(range(w.num_seqs))
     for i in range(args.warmup):
-        _oracle_seq(w, order[i % len(order)])
+        _oracle_seq(w, order[i % len(order)], None, cores)
     done_bytes = 0
     s0 = time.perf_counter()
     for i in range(args.steps):
         s = order[i % len(order)]
-        _oracle_seq(w, s)
+        _oracle_seq(w, s, None, cores)
         done_bytes += seq_kv_bytes(w, s)
     el = time.perf_counter() - s0
     value = done_bytes / el / 1e9
-    cores = oracle.max_threads()
     ms = el * 1e3 / args.steps
     line = {
         "impl": "reference",
@@ -684,10 +847,11 @@ def run_reference(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
-        "config": describe(w, args.config, part),
+        "config": describe(w, cfg, part),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": "one sequence of the batch (all its query heads) per step, "
-                                   "cycling through the batch; fp64 C oracle, OpenMP"},
+                                   "cycling through the batch; fp64 C oracle, OpenMP",
+                         "cpu": cpu},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -808,14 +972,50 @@ def tensor_peak() -> tuple[float, str]:
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def _oracle_prefill_seq(w, s):
+def _oracle_prefill_seq(w, s, threads: int = 0):
     """The oracle on sequence s alone (all its chunk rows)."""
     import oracle
 
     a, b = int(w.query_start[s]), int(w.query_start[s + 1])
     return oracle.paged_prefill(w.chunk_q[a:b], w.k_cache, w.v_cache, w.block_tables[s:s + 1],
                                 w.context_lens[s:s + 1], np.array([0, b - a], np.int32), w.scale,
-                                w.dtype)
+                                w.dtype, num_threads=threads)
+
+
+def _oracle_prefill_head_rows(w, s, r: int, threads: int) -> int:
+    """The oracle on the first ``r`` chunk rows of sequence s; returns their flops.
+
+    Rows 0..r-1 of a chunk of n tokens over L cached tokens attend positions 0..L-n+i,
+    which is the chunk of r tokens over L-n+r cached tokens: the same arithmetic."""
+    import oracle
+
+    a, b = int(w.query_start[s]), int(w.query_start[s + 1])
+    r = min(r, b - a)
+    Lr = int(w.context_lens[s]) - (b - a) + r
+    oracle.paged_prefill(w.chunk_q[a:a + r], w.k_cache, w.v_cache, w.block_tables[s:s + 1],
+                         np.array([Lr], np.int32), np.array([0, r], np.int32), w.scale, w.dtype,
+                         num_threads=threads)
+    keys = (Lr - r) * r + r * (r + 1) // 2
+    return 4 * w.head_dim * w.num_q_heads * keys
+
+
+def _oracle_prefill_rate(w, seconds: float, threads: int, max_seqs: int, rows: int = 0):
+    """TFLOP/s of the prefill oracle over whole sequences (or their first ``rows`` chunk
+    rows) until ``seconds`` pass."""
+    done, nseq = 0, 0
+    s0 = time.perf_counter()
+    while True:
+        s = nseq % w.num_seqs
+        if rows:
+            done += _oracle_prefill_head_rows(w, s, rows, threads)
+        else:
+            _oracle_prefill_seq(w, s, threads)
+            done += prefill_flops(w, [s])
+        nseq += 1
+        el = time.perf_counter() - s0
+        if el >= seconds or nseq >= max_seqs:
+            break
+    return done / el / 1e12, nseq, el
 
 
 def prefill_config(w) -> dict:
@@ -846,12 +1046,14 @@ def run_prefill(args) -> None:
         import oracle
 
         oracle.build()
+        cpu = host_cpu()
+        cores = cpu["usable_cores"]
         for i in range(args.warmup):
-            _oracle_prefill_seq(w, i % w.num_seqs)
+            _oracle_prefill_seq(w, i % w.num_seqs, cores)
         flops = 0
         s0 = time.perf_counter()
         for i in range(args.steps):
-            _oracle_prefill_seq(w, i % w.num_seqs)
+            _oracle_prefill_seq(w, i % w.num_seqs, cores)
             flops += prefill_flops(w, [i % w.num_seqs])
         el = time.perf_counter() - s0
         value = flops / el / 1e12
@@ -862,9 +1064,9 @@ def run_prefill(args) -> None:
                 "data": "synthetic (seeded N(0,1) q/K/V, shuffled block pool)",
                 "config": prefill_config(w),
                 "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
-                                 "cores": oracle.max_threads(), "kind": "oracle",
+                                 "cores": cores, "kind": "oracle",
                                  "sample": "one sequence's whole chunk per step, cycling through "
-                                           "the batch; fp64 C oracle, OpenMP"},
+                                           "the batch; fp64 C oracle, OpenMP", "cpu": cpu},
                 "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -942,20 +1144,17 @@ def run_prefill(args) -> None:
         import oracle
 
         oracle.build()
-        done, nseq = 0, 0
-        s0 = time.perf_counter()
-        while True:
-            s = nseq % w.num_seqs
-            _oracle_prefill_seq(w, s)
-            done += prefill_flops(w, [s])
-            nseq += 1
-            el = time.perf_counter() - s0
-            if el >= args.cpu_seconds or nseq >= w.num_seqs:
-                break
-        cpu = {"value": round(done / el / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
-               "kind": "oracle",
-               "sample": f"{nseq} sequences' whole chunks in {el:.1f} s; fp64 C oracle, OpenMP "
-                         f"over (query row, head)"}
+        hc = host_cpu()
+        cores = hc["usable_cores"]
+        v1, n1, e1 = _oracle_prefill_rate(w, args.cpu_seconds / 2, 1, w.num_seqs, rows=16)
+        vn, nn, en = _oracle_prefill_rate(w, args.cpu_seconds, cores, w.num_seqs)
+        cpu = {"value": round(vn, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{nn} sequences' whole chunks in {en:.1f} s on {cores} threads; fp64 "
+                         f"C oracle, OpenMP over (query row, head)",
+               "single_thread": {"value": round(v1, 6), "unit": "TFLOP/s", "cores": 1,
+                                 "sample": f"the first 16 chunk rows of {n1} sequences in "
+                                           f"{e1:.1f} s on one thread"},
+               "cpu": hc}
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     PKV_DERR_PAIR,
     PKV_DERR_SLOT,
     PKV_DERR_TIMEOUT,
+    PKV_ENODEVMEM,
     PKV_ESCRATCH,
     PKV_F16,
     PKV_F32,

@@ -24,6 +24,7 @@ PKV_DERR_PAIR = 4
 PKV_DERR_CONTEXT = 8
 PKV_DERR_TIMEOUT = 16
 PKV_ESCRATCH = -5
+PKV_ENODEVMEM = -6
 
 _lock = threading.Lock()
 _lib = None
@@ -162,20 +163,31 @@ def paged_attn_decode_partition_tokens(num_seqs: int, num_q_heads: int, num_kv_h
     return rc
 
 
-def workspace_for(device, nbytes: int) -> torch.Tensor | None:
+def _reuse(key, nbytes: int, alloc):
+    """The cached buffer under ``key`` if it holds ``nbytes``, else a new one from
+    ``alloc(nbytes)``, which replaces it in the cache."""
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = alloc(nbytes)
+        _workspaces[key] = buf
+    return buf
+
+
+def workspace_for(device, nbytes: int, stream=None) -> torch.Tensor | None:
     """A byte buffer of at least ``nbytes`` on ``device``, reused across calls.
 
-    The library clears what it needs in the workspace at every call, so one buffer
-    serves every call made on one stream, whatever the shapes.
+    One buffer is kept per (device, stream): calls on one stream run in order, and every
+    call writes each workspace byte it reads, so they can share a buffer whatever their
+    shapes.  Calls on different streams may overlap on the GPU and get different
+    buffers.  ``stream`` is a torch.cuda.Stream, a raw handle, or None for the current
+    stream.  A caller that passes the same explicit ``workspace`` to calls on different
+    streams must order those calls itself.
     """
     if nbytes == 0:
         return None
-    key = torch.device(device)
-    buf = _workspaces.get(key)
-    if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(nbytes, dtype=torch.uint8, device=key)
-        _workspaces[key] = buf
-    return buf
+    dev = torch.device(device)
+    return _reuse((dev, _stream(stream)), nbytes,
+                  lambda n: torch.empty(n, dtype=torch.uint8, device=dev))
 
 
 def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
@@ -200,7 +212,7 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
     MB = block_tables.shape[1]
     need = paged_attn_decode_workspace_size(B, Hq, Hkv, D, bs, MB, partition_size)
     if workspace is None:
-        workspace = workspace_for(q.device, need)
+        workspace = workspace_for(q.device, need, stream)
     ws_ptr = _cuda("workspace", workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = load().paged_attn_decode(
@@ -283,7 +295,7 @@ def paged_attn_decode_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache:
     need = paged_attn_decode_shared_prefix_workspace_size(B, G, Hq, Hkv, bs, block_tables.shape[1],
                                                           max_group_size, max_prefix_tokens)
     if workspace is None:
-        workspace = workspace_for(q.device, need)
+        workspace = workspace_for(q.device, need, stream)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = load().paged_attn_decode_shared_prefix(
         _cuda("out", out), _cuda("q", q), _cuda("k_cache", k_cache), _cuda("v_cache", v_cache),
@@ -414,7 +426,7 @@ def paged_attn_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Ten
     MB = block_tables.shape[1]
     need = paged_attn_decode_workspace_size(B, Hq, Hkv, D, bs, MB, partition_size)
     if workspace is None:
-        workspace = workspace_for(q.device, need)
+        workspace = workspace_for(q.device, need, stream)
     ws_ptr = _cuda("workspace", workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = load().paged_attn_decode_fp8(

@@ -381,6 +381,7 @@ const char* pkv_strerror(int code) {
     case PKV_ECUDA: return "CUDA runtime error";
     case PKV_EUNSUPPORTED: return "unsupported head_dim / block_size / dtype combination";
     case PKV_ESCRATCH: return "problem needs more scratch than the no-alloc decode provides";
+    case PKV_ENODEVMEM: return "no device memory left to load the no-alloc decode's scratch array";
     case static_cast<int>(PKV_DERR_BLOCK_ID): return "device: block id out of range";
     case static_cast<int>(PKV_DERR_SLOT): return "device: slot out of range";
     case static_cast<int>(PKV_DERR_PAIR): return "device: copy pair id out of range";

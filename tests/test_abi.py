@@ -151,3 +151,31 @@ def test_binding_argument_lists_match_the_header():
         if fn.argtypes is None:
             continue
         assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), len(params))
+
+
+def test_workspace_cache_keeps_one_buffer_per_device_and_stream(monkeypatch):
+    # calls on one stream share a buffer; a call on another stream gets its own, so two
+    # decodes issued on different streams never write the same workspace
+    import torch
+
+    from paged_kv_cache_315_gb300 import _binding as b
+
+    monkeypatch.setattr(b, "_workspaces", {})
+    made = []
+
+    def alloc(n):
+        made.append(n)
+        return torch.empty(n, dtype=torch.uint8)
+
+    dev = torch.device("cuda", 0)
+    a1 = b._reuse((dev, 111), 64, alloc)
+    a2 = b._reuse((dev, 111), 32, alloc)          # smaller request on the same stream
+    c1 = b._reuse((dev, 222), 64, alloc)          # another stream
+    d1 = b._reuse((torch.device("cuda", 1), 111), 64, alloc)  # another device
+    assert a1 is a2
+    assert c1 is not a1 and d1 is not a1 and d1 is not c1
+    a3 = b._reuse((dev, 111), 128, alloc)         # grows in place of the old one
+    assert a3 is not a1 and a3.numel() == 128
+    assert b._reuse((dev, 111), 100, alloc) is a3
+    assert made == [64, 64, 64, 128]
+    assert set(b._workspaces) == {(dev, 111), (dev, 222), (torch.device("cuda", 1), 111)}

@@ -590,3 +590,48 @@ def test_fp8_config3_gqa_full_size(pkv):
     ref = oracle.paged_decode_fp8kv(w.q[seqs], k8, v8, w.block_tables[seqs], w.context_lens[seqs],
                                     w.scale, ks, vs, "bf16")
     assert_close(host_out(out)[seqs], ref, "bf16", "fp8 config 3")
+
+
+@pytest.mark.parametrize("cfg", [2, 4, 5])
+def test_fp8_full_size_benchmark_batches(pkv, cfg):
+    """E4M3 caches on the decode batches bench.py times with --kv-dtype fp8, with its
+    scales, cache state, per-step writes and partition size: sampled sequences (always
+    the longest and the shortest) against the oracle, and the caches byte for byte."""
+    import bench
+
+    w = bench.bench_workload(cfg)
+    ks, vs = bench.fp8_scales(cfg)
+    k8, v8, t = _fp8_setup(w, ks, vs)
+    if cfg == 4:
+        # the batch's state: copy-on-write copies, then every suffix token
+        sk = synth.storage_to_torch(w.info["setup_k"], "bf16", "cuda")
+        sv = synth.storage_to_torch(w.info["setup_v"], "bf16", "cuda")
+        ss = torch.from_numpy(w.info["setup_slots"]).cuda()
+        pkv.kv_copy_blocks(t["k8"], t["copy_pairs"])
+        pkv.kv_copy_blocks(t["v8"], t["copy_pairs"])
+        pkv.kv_cache_write_fp8(sk, sv, t["k8"], t["v8"], ss, ks, vs)
+        oracle.copy_blocks(k8, w.copy_pairs)
+        oracle.copy_blocks(v8, w.copy_pairs)
+        assert oracle.kv_cache_write_fp8(w.info["setup_k"], w.info["setup_v"], k8, v8,
+                                         w.info["setup_slots"], ks, vs, "bf16") == 0
+        # one step: the copies again, then each sequence's next token
+        pkv.kv_copy_blocks(t["k8"], t["copy_pairs"])
+        pkv.kv_copy_blocks(t["v8"], t["copy_pairs"])
+        oracle.copy_blocks(k8, w.copy_pairs)
+        oracle.copy_blocks(v8, w.copy_pairs)
+    pkv.kv_cache_write_fp8(t["k_new"], t["v_new"], t["k8"], t["v8"], t["slot_mapping"], ks, vs)
+    assert oracle.kv_cache_write_fp8(w.k_new, w.v_new, k8, v8, w.slot_mapping, ks, vs,
+                                     "bf16") == 0
+    part = pkv.paged_attn_decode_partition_tokens(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                  w.block_size, w.max_blocks_per_seq,
+                                                  w.partition_size)
+    out = torch.empty_like(t["q"])
+    pkv.paged_attn_decode_fp8(out, t["q"], t["k8"], t["v8"], t["block_tables"], t["context_lens"],
+                              w.scale, ks, vs, partition_size=part)
+    assert pkv.pkv_device_error() == 0
+    assert np.array_equal(t["k8"].cpu().numpy(), k8)
+    assert np.array_equal(t["v8"].cpu().numpy(), v8)
+    seqs = _sample(w, 3 if cfg == 5 else 16, 20 + cfg)
+    ref = oracle.paged_decode_fp8kv(w.q[seqs], k8, v8, w.block_tables[seqs], w.context_lens[seqs],
+                                    w.scale, ks, vs, "bf16")
+    assert_close(host_out(out)[seqs], ref, "bf16", f"fp8 config {cfg}")

@@ -161,13 +161,15 @@ def test_prefill_reports_bad_chunks_and_block_ids(pkv):
     assert_close(out.float().cpu().numpy(), ref, "after errors")
 
 
-def test_prefill_batch_full_size_sampled_rows(pkv):
-    """The chunked-prefill batch at full size, in the launch bench.py times.
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_prefill_batch_full_size_sampled_rows(pkv, head_dim):
+    """The chunked-prefill batch at full size (bench.py --op prefill [--head-dim 64]), in
+    the launch bench.py times.
 
     Sampled rows are checked one by one: row i of a chunk is a decode query over the
     first L - n + i + 1 tokens (a pinned property of the oracle).
     """
-    w = synth.prefill_workload()
+    w = synth.prefill_workload(head_dim=head_dim)
     t = synth.to_torch(w, "cuda")
     out = gpu_prefill(pkv, w, t).float().cpu().numpy()
     assert pkv.pkv_device_error() == 0

@@ -145,3 +145,27 @@ def test_grouped_prompts_match_oracle(pkv):
     ref = oracle.paged_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
                               w.dtype)
     assert_close(out, ref, "grouped prompts")
+
+
+def test_grouped_prompts_full_size_in_the_benchmarked_launch(pkv):
+    """The grouped-prompt batch bench.py times with --grouped-prefix --shared-prefix (64
+    prompts of 4096 tokens x 8 samples), after the step's slot write, in that launch:
+    sampled sequences (the longest, the shortest and one whole group) against the oracle."""
+    w = synth.grouped_prefix_workload()
+    synth.add_new_tokens(w, seed=synth.BASE_SEED + 107)
+    t = synth.to_torch(w, "cuda")
+    pkv.kv_cache_write(t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], t["slot_mapping"])
+    gs, pls = w.info["group_start"], w.info["prefix_lens"]
+    out = cascade(pkv, w, t, gs.tolist(), pls.tolist())
+    assert pkv.pkv_device_error() == 0
+    assert np.isfinite(out).all()
+    k, v = w.k_cache.copy(), w.v_cache.copy()
+    assert oracle.kv_cache_write(w.k_new, w.v_new, k, v, w.slot_mapping) == 0
+    rng = np.random.default_rng(7)
+    g = int(rng.integers(0, len(pls)))
+    seqs = np.unique(np.r_[np.argmax(w.context_lens), np.argmin(w.context_lens),
+                           np.arange(gs[g], gs[g + 1]),
+                           rng.choice(w.num_seqs, 16, replace=False)])
+    ref = oracle.paged_decode(w.q[seqs], k, v, w.block_tables[seqs], w.context_lens[seqs],
+                              w.scale, w.dtype)
+    assert_close(out[seqs], ref, "grouped prompts, full size")
