@@ -186,7 +186,8 @@ int kv_cache_write(const void* k, const void* v, void* k_cache, void* v_cache,
  *                query_start[num_seqs] = num_q_tokens.
  *   max_query_len  an upper bound on every n_s (sizes the grid; host value).
  * All pointers are caller-owned device memory; the call is asynchronous on `stream` and
- * allocates nothing.  head_dim 64 or 128, block_size 16, 32 or 64.
+ * allocates nothing.  head_dim 64 or 128, block_size 16, 32 or 64, any finite scale (a
+ * negative one is computed exactly as (-q) . k times |scale|).
  * Device-side data errors set PKV_DERR_* bits (see pkv_device_error) and skip the unit:
  * a chunk longer than its context or than max_query_len, a context longer than the table
  * or rows outside [0, num_q_tokens) set PKV_DERR_CONTEXT and leave that sequence's rows
@@ -214,7 +215,7 @@ int paged_attn_prefill(void* out, const void* q, const void* k_cache, const void
  *
  *   out, q, k_cache, v_cache, block_tables, context_lens, num_seqs, ..., dtype:
  *                as in paged_attn_decode (dtype PKV_BF16 or PKV_F16, head_dim 128,
- *                block_size 16, 32 or 64, scale > 0).
+ *                block_size 16, 32 or 64, any finite scale).
  *   group_start  int32 [num_groups + 1], device: group g is the run of sequences
  *                group_start[g] .. group_start[g+1]-1 (non-decreasing, within
  *                [0, num_seqs]); sequences outside every run have no shared prefix.

@@ -107,7 +107,8 @@ def test_argument_checks_return_before_any_cuda_call(lib):
         ctypes.c_int(dt), null, ctypes.c_size_t(0), null)
     assert sp(*spargs(8, 2, 64, 16, 1, 0.1)) == -4     # head_dim 64 not served
     assert sp(*spargs(12, 4, 128, 16, 1, 0.1)) == -1   # 3 heads per KV head: served (null ptrs)
-    assert sp(*spargs(8, 2, 128, 16, 1, -0.1)) == -4   # negative scale not served
+    assert sp(*spargs(8, 2, 128, 16, 1, -0.1)) == -1   # negative scale: served (null ptrs)
+    assert sp(*spargs(8, 2, 128, 16, 1, float("nan"))) == -4   # NaN scale not served
     assert sp(*spargs(8, 2, 128, 16, 1, 0.1)) == -1    # null pointers
     ws = lib.paged_attn_decode_shared_prefix_workspace_size
     ws.restype = ctypes.c_size_t

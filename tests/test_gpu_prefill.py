@@ -84,18 +84,21 @@ def test_prefill_matches_oracle(pkv, dtype, Hq, Hkv, D, bs):
                  f"{dtype} Hq{Hq} Hkv{Hkv} D{D} bs{bs}")
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_prefill_negative_scale_matches_oracle(pkv, D):
-    # a scale that is not positive takes the mma.sync kernel (the tcgen05 kernel folds a
-    # positive scale into its exponent after taking the maximum of the raw scores)
-    w = synth.make_prefill_workload("pfn", seed=16 + D, dtype="bf16", prior_lens=[0, 40, 130],
-                                    chunk_lens=[17, 64, 9], num_q_heads=8, num_kv_heads=2,
-                                    head_dim=D, block_size=16)
-    w.scale = -w.scale
+@pytest.mark.parametrize("D,mult,Hq,Hkv", [(64, -1.0, 8, 2), (128, -1.0, 8, 2),
+                                            (128, -2.5, 12, 4), (128, 0.0, 8, 2),
+                                            (64, 0.0, 6, 3), (128, 0.0, 12, 4)])
+def test_prefill_non_positive_scale_matches_oracle(pkv, D, mult, Hq, Hkv):
+    # a negative scale runs as (-q) . k times |scale| (query rows staged with flipped
+    # signs); a zero scale weighs every attended key 1, and keys past a row's causal limit
+    # must still weigh 0
+    w = synth.make_prefill_workload("pfn", seed=16 + D + Hq, dtype="bf16",
+                                    prior_lens=[0, 40, 130], chunk_lens=[17, 64, 9],
+                                    num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=16)
+    w.scale = mult * w.scale
     t = synth.to_torch(w, "cuda")
     out = gpu_prefill(pkv, w, t)
     assert pkv.pkv_device_error() == 0
-    assert_close(out.float().cpu().numpy(), oracle_prefill(w), f"negative scale D{D}")
+    assert_close(out.float().cpu().numpy(), oracle_prefill(w), f"scale {w.scale} D{D} Hq{Hq}")
 
 
 def test_prefill_of_one_token_chunks_matches_decode_oracle(pkv):

@@ -79,6 +79,22 @@ def test_groups_of_mixed_sizes_match_oracle(pkv, Hq, Hkv, bs, dtype):
     assert (out[9] == 0).all()  # empty context
 
 
+@pytest.mark.parametrize("mult", [-1.0, 0.0])
+def test_cascade_with_a_non_positive_scale_matches_oracle(pkv, mult):
+    # the prefix pass runs (-q) . k times |scale| for a negative scale; the suffix pass and
+    # the merge take the scale as it is
+    w = synth.make_workload("spn", seed=41, dtype="bf16", context_lens=[200, 77, 129, 64, 300],
+                            num_q_heads=16, num_kv_heads=4, head_dim=128, block_size=16)
+    share_prefix(w, [0, 3, 5], [64, 48])
+    w.scale = mult * w.scale
+    t = synth.to_torch(w, "cuda")
+    out = cascade(pkv, w, t, [0, 3, 5], [64, 48])
+    assert pkv.pkv_device_error() == 0
+    ref = oracle.paged_decode(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                              w.dtype)
+    assert_close(out, ref, f"cascade, scale {w.scale}")
+
+
 def test_one_group_with_a_long_prefix_splits_its_keys(pkv):
     # 24 sequences share a 2048-token prefix: the prefix pass splits the keys across CTAs
     lens = 2048 + np.arange(24) * 37 % 300
