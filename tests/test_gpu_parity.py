@@ -146,6 +146,8 @@ SHAPES = [
     ("f32", 12, 1, 32, 16, 48),
     ("bf16", 4, 2, 256, 16, 128),    # CUDA-core path for 16-bit types
     ("bf16", 16, 4, 128, 8, 64),     # block_size 8: CUDA-core path
+    ("bf16", 32, 8, 128, 64, 256),   # 64-token blocks staged as four 16-token slices
+    ("f16", 12, 4, 128, 32, 0),      # 32-token blocks as two slices, 3 heads per KV head
 ]
 
 
@@ -248,7 +250,8 @@ def test_physical_block_permutation_gives_identical_bits(pkv):
     assert torch.equal(out, base)
 
 
-@pytest.mark.parametrize("dtype,D,bs", [("bf16", 128, 16), ("bf16", 64, 32), ("f32", 64, 16)])
+@pytest.mark.parametrize("dtype,D,bs", [("bf16", 128, 16), ("bf16", 64, 32), ("f32", 64, 16),
+                                        ("bf16", 128, 32), ("bf16", 128, 64)])
 def test_poisoned_dead_slots_and_table_tail_are_never_read(pkv, dtype, D, bs):
     w = synth.make_workload("n", seed=10, dtype=dtype, context_lens=[1, bs - 3, bs + 1, 301],
                             num_q_heads=8, num_kv_heads=2, head_dim=D, block_size=bs,
