@@ -315,8 +315,8 @@ __device__ __forceinline__ void online_softmax(float (&sc)[BS / 8][4], float (&o
   float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const uint32_t lo = Mma<T>::pack(exp2f(sc[nt][0] - mn0), exp2f(sc[nt][1] - mn0));
-    const uint32_t hi = Mma<T>::pack(exp2f(sc[nt][2] - mn1), exp2f(sc[nt][3] - mn1));
+    const uint32_t lo = Mma<T>::pack(fast_exp2(sc[nt][0] - mn0), fast_exp2(sc[nt][1] - mn0));
+    const uint32_t hi = Mma<T>::pack(fast_exp2(sc[nt][2] - mn1), fast_exp2(sc[nt][3] - mn1));
     const float2 flo = Mma<T>::unpack(lo), fhi = Mma<T>::unpack(hi);
     rs0 += flo.x + flo.y;
     rs1 += fhi.x + fhi.y;
@@ -324,7 +324,7 @@ __device__ __forceinline__ void online_softmax(float (&sc)[BS / 8][4], float (&o
     pa[nt >> 1][(nt & 1) * 2 + 1] = hi;
   }
   if (__any_sync(0xffffffffu, up0 || up1)) {
-    const float a0 = exp2f(m[0] - mn0), a1 = exp2f(m[1] - mn1);  // 1 for rows that kept m
+    const float a0 = fast_exp2(m[0] - mn0), a1 = fast_exp2(m[1] - mn1);  // 1 for rows that kept m
     l[0] *= a0;
     l[1] *= a1;
 #pragma unroll
@@ -878,8 +878,8 @@ __device__ __forceinline__ void tcg_block(uint32_t kb, uint32_t vb, const uint32
   float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
-    const uint32_t lo = Mma<T>::pack(exp2f(sc[mt][0] - mn0), exp2f(sc[mt][1] - mn1));
-    const uint32_t hi = Mma<T>::pack(exp2f(sc[mt][2] - mn0), exp2f(sc[mt][3] - mn1));
+    const uint32_t lo = Mma<T>::pack(fast_exp2(sc[mt][0] - mn0), fast_exp2(sc[mt][1] - mn1));
+    const uint32_t hi = Mma<T>::pack(fast_exp2(sc[mt][2] - mn0), fast_exp2(sc[mt][3] - mn1));
     const float2 flo = Mma<T>::unpack(lo), fhi = Mma<T>::unpack(hi);
     rs0 += flo.x + fhi.x;
     rs1 += flo.y + fhi.y;
@@ -887,7 +887,7 @@ __device__ __forceinline__ void tcg_block(uint32_t kb, uint32_t vb, const uint32
     pb[mt][1] = movmatrix_trans(hi);  // (head r8, tokens 8 + 2c, 9 + 2c)
   }
   if (__any_sync(0xffffffffu, up0 || up1)) {
-    const float a0 = exp2f(m[0] - mn0), a1 = exp2f(m[1] - mn1);
+    const float a0 = fast_exp2(m[0] - mn0), a1 = fast_exp2(m[1] - mn1);
     l[0] *= a0;
     l[1] *= a1;
 #pragma unroll
@@ -1084,8 +1084,8 @@ __device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint3
   float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
-    const uint32_t lo = Mma<__half>::pack(exp2f(sc[mt][0] - mn0), exp2f(sc[mt][1] - mn1));
-    const uint32_t hi = Mma<__half>::pack(exp2f(sc[mt][2] - mn0), exp2f(sc[mt][3] - mn1));
+    const uint32_t lo = Mma<__half>::pack(fast_exp2(sc[mt][0] - mn0), fast_exp2(sc[mt][1] - mn1));
+    const uint32_t hi = Mma<__half>::pack(fast_exp2(sc[mt][2] - mn0), fast_exp2(sc[mt][3] - mn1));
     const float2 flo = Mma<__half>::unpack(lo), fhi = Mma<__half>::unpack(hi);
     rs0 += flo.x + fhi.x;
     rs1 += flo.y + fhi.y;
@@ -1093,7 +1093,7 @@ __device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint3
     pb[mt][1] = movmatrix_trans(hi);  // (head r8, tokens 8 + 2c, 9 + 2c)
   }
   if (__any_sync(0xffffffffu, up0 || up1)) {
-    const float a0 = exp2f(m[0] - mn0), a1 = exp2f(m[1] - mn1);  // 1 for heads that kept m
+    const float a0 = fast_exp2(m[0] - mn0), a1 = fast_exp2(m[1] - mn1);  // 1 for heads that kept m
     l[0] *= a0;
     l[1] *= a1;
 #pragma unroll

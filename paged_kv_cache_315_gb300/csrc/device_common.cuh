@@ -26,6 +26,14 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// 2^x by the hardware approximation (MUFU.EX2, relative error about 2^-22; results below
+// the normal range flush to 0), for softmax weights that are rounded to 16 bits anyway.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }

@@ -48,13 +48,6 @@ struct PrefillParams {
   int ksplit;                 // key ranges per sequence (non-causal only), one partial each
 };
 
-// 2^x by the hardware approximation (MUFU.EX2; results below the normal range flush to 0).
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // two fp32 lanes in one 64-bit register: packed FMA and add (sm_100 and later)
 __device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
   unsigned long long r;
