@@ -48,16 +48,17 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # workload and partition size, valid only for the kernel source whose hash is recorded
 # beside it (profiles/ holds the captures).
 MEASURED_TRAFFIC: dict = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each
-    "13b-mha-b64-bf16@2048": {"bytes": 1408908544 + 3557632, "decode_cu_sha": "c33ade031646219c"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963425536 + 6619904, "decode_cu_sha": "c33ade031646219c"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328653824 + 5491968, "decode_cu_sha": "c33ade031646219c"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4296349440 + 40238592, "decode_cu_sha": "c33ade031646219c"},
-    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704758272 + 3695360, "decode_cu_sha": "c33ade031646219c"},
-    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483133184 + 5581824, "decode_cu_sha": "c33ade031646219c"},
-    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164988160 + 5210624, "decode_cu_sha": "c33ade031646219c"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148133632 + 34915840, "decode_cu_sha": "c33ade031646219c"},
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 2102498560, "decode_cu_sha": "c33ade031646219c"},
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each (the
+    # timed step of `bench.py --steps 1 --warmup 3`)
+    "13b-mha-b64-bf16@2048": {"bytes": 1408769792 + 668672, "decode_cu_sha": "b160b5674f9dae30"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963336192 + 3542016, "decode_cu_sha": "b160b5674f9dae30"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328343040 + 2344960, "decode_cu_sha": "b160b5674f9dae30"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4296091136 + 37296640, "decode_cu_sha": "b160b5674f9dae30"},
+    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704751872 + 625664, "decode_cu_sha": "b160b5674f9dae30"},
+    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483123712 + 2494208, "decode_cu_sha": "b160b5674f9dae30"},
+    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164948992 + 2191616, "decode_cu_sha": "b160b5674f9dae30"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148129792 + 31825664, "decode_cu_sha": "b160b5674f9dae30"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1992766720 + 25097472, "decode_cu_sha": "b160b5674f9dae30"},
 }
 
 
@@ -244,8 +245,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393096448, "sources_sha": "ec44e244c4cbafe9"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 354257408, "sources_sha": "ec44e244c4cbafe9"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393143040, "sources_sha": "e1d88619f3faa3db"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 354289152, "sources_sha": "e1d88619f3faa3db"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 
@@ -934,21 +935,27 @@ def run_swap(args) -> None:
 # ------------------------------------------------------------------------------------------
 
 # DRAM bytes (read + write) per launch of the chunked-prefill kernel on the chunked-prefill
-# batch, from one ncu capture, valid only for the kernel source whose hash is recorded.
-PREFILL_TRAFFIC = {"workload": "chunked-prefill-70b-gqa8-c512", "bytes": 278724608 + 106193664,
-                   "prefill_cu_sha": "4d7a49772f687c7e"}
+# batches (head_dim 128 and 64), from one ncu capture each, valid only for the kernel source
+# whose hash is recorded.
+PREFILL_TRAFFIC = {
+    "chunked-prefill-70b-gqa8-c512": {"bytes": 278784256 + 103175424,
+                                      "prefill_cu_sha": "cad756ccb9424f88"},
+    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139377664 + 36586496,
+                                          "prefill_cu_sha": "cad756ccb9424f88"},
+}
 
 
 def prefill_traffic(w_name: str) -> float | None:
-    """Recorded DRAM bytes of the benchmark prefill batch (head_dim 128) for the recorded
-    prefill.cu, else None."""
+    """Recorded DRAM bytes of a benchmark prefill batch for the recorded prefill.cu, else
+    None."""
     import hashlib
 
-    if w_name != PREFILL_TRAFFIC["workload"]:
+    entry = PREFILL_TRAFFIC.get(w_name)
+    if not entry:
         return None
     src = os.path.join(ROOT, "paged_kv_cache_315_gb300", "csrc", "prefill.cu")
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return float(PREFILL_TRAFFIC["bytes"]) if PREFILL_TRAFFIC["prefill_cu_sha"] == digest else None
+    return float(entry["bytes"]) if entry["prefill_cu_sha"] == digest else None
 
 
 def prefill_flops(w: synth.Workload, seqs=None) -> int:
