@@ -241,9 +241,9 @@ __global__ void __launch_bounds__(kUThreads, 2)
                       q0 + row0 / G);
       }
     }
-    int issued = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      const int st = j % kUStages;
+    // TMA row coordinate of lane k's block of tile j (out of range, so reading zeros, past
+    // the context); the next tile's is read while this one waits for its slot
+    auto row_of = [&](int j) -> int {
       int y = P.num_blocks * BS;
       if (lane < NBT) {
         const int jb = blk0 + j * NBT + lane;
@@ -255,6 +255,14 @@ __global__ void __launch_bounds__(kUThreads, 2)
             raise_error(P.err, PKV_DERR_BLOCK_ID);
         }
       }
+      return y;
+    };
+    int issued = 0;
+    int ynext = ntiles > 0 ? row_of(0) : 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % kUStages;
+      const int y = ynext;
+      if (j + 1 < ntiles) ynext = row_of(j + 1);
       int ok = 1;
       if (lane == 0 && j >= kUStages)
         ok = mbar_wait_bounded(smem_addr(&emptyb[st]), ((j / kUStages) - 1) & 1) ? 1 : 0;
@@ -282,7 +290,9 @@ __global__ void __launch_bounds__(kUThreads, 2)
     if (lane == 0) flags[is_k ? 1 : 2] = issued;
   } else if (warp == 5) {
     // ---- MMA issuer -----------------------------------------------------------------------
-    const uint32_t qb = smem_addr(sq);
+    // K-step 0 of Q (a K-step adds its byte offset / 16 to the start-address field; every
+    // address stays below 256 KB, so no carry leaves it)
+    const uint64_t dq = smem_desc_sw128(smem_addr(sq), 16, 1024);
     int ok = 1;
     if (lane == 0) ok = mbar_wait_bounded(smem_addr(q_full), 0) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -314,7 +324,8 @@ __global__ void __launch_bounds__(kUThreads, 2)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      const uint32_t vb = smem_addr(vt);
+      // K-step 0 of V; a K-step adds its byte offset / 16 to the start-address field
+      const uint64_t dv = smem_desc_sw128(smem_addr(vt), kUKeys * 128, 1024);
       if constexpr (WI) {
         // the whole (converged) warp runs the issue; lane 0 performs it
         const uint32_t iss = lane == 0;
@@ -322,7 +333,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
 #pragma unroll
         for (int kt = 0; kt < kUKeys / 16; ++kt)
           umma_ts_warp(iss, tm_o, tm + b * kUKeys + kt * 8,
-                       smem_desc_sw128(vb + kt * 2048, kUKeys * 128, 1024), kIdPV,
+                       dv + static_cast<uint64_t>(kt * 128), kIdPV,
                        (i > 0 || kt > 0) ? 1u : 0u);
         umma_commit_warp(iss, smem_addr(&v_empty[st]));
         umma_commit_warp(iss, smem_addr(pv_done));
@@ -331,7 +342,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
 #pragma unroll
         for (int kt = 0; kt < kUKeys / 16; ++kt)
           umma_ts(tm_o, tm + b * kUKeys + kt * 8,
-                  smem_desc_sw128(vb + kt * 2048, kUKeys * 128, 1024), kIdPV,
+                  dv + static_cast<uint64_t>(kt * 128), kIdPV,
                   (i > 0 || kt > 0) ? 1u : 0u);
         umma_commit(smem_addr(&v_empty[st]));
         umma_commit(smem_addr(pv_done));
@@ -360,15 +371,15 @@ __global__ void __launch_bounds__(kUThreads, 2)
           break;
         }
       }
-      const uint32_t kb = smem_addr(ring + st * 2 * kUTile);
+      const uint64_t dk = smem_desc_sw128(smem_addr(ring + st * 2 * kUTile), 16, 1024);
       if constexpr (WI) {
         const uint32_t iss = lane == 0;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss_warp(iss, tm + b * kUKeys,
-                       smem_desc_sw128(qb + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024),
-                       smem_desc_sw128(kb + (kk >> 2) * (kUKeys * 128) + (kk & 3) * 32, 16, 1024),
+                       dq + static_cast<uint64_t>(((kk >> 2) * (kURows * 128) + (kk & 3) * 32) >> 4),
+                       dk + static_cast<uint64_t>(((kk >> 2) * (kUKeys * 128) + (kk & 3) * 32) >> 4),
                        kIdQK, kk > 0 ? 1u : 0u);
         umma_commit_warp(iss, smem_addr(&k_empty[st]));
         umma_commit_warp(iss, smem_addr(&s_full[b]));
@@ -377,8 +388,8 @@ __global__ void __launch_bounds__(kUThreads, 2)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           umma_ss(tm + b * kUKeys,
-                  smem_desc_sw128(qb + (kk >> 2) * (kURows * 128) + (kk & 3) * 32, 16, 1024),
-                  smem_desc_sw128(kb + (kk >> 2) * (kUKeys * 128) + (kk & 3) * 32, 16, 1024),
+                  dq + static_cast<uint64_t>(((kk >> 2) * (kURows * 128) + (kk & 3) * 32) >> 4),
+                  dk + static_cast<uint64_t>(((kk >> 2) * (kUKeys * 128) + (kk & 3) * 32) >> 4),
                   kIdQK, kk > 0 ? 1u : 0u);
         umma_commit(smem_addr(&k_empty[st]));
         umma_commit(smem_addr(&s_full[b]));
