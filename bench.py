@@ -434,10 +434,13 @@ def decode_session(args, cfg: int, dev, pkv):
     out = torch.empty_like(t["q"])
     B = w.num_seqs
     part = w.partition_size if args.partition < 0 else args.partition
-    part = pkv.paged_attn_decode_partition_tokens(B, w.num_q_heads, w.num_kv_heads, w.block_size,
-                                                  w.max_blocks_per_seq, part)
-    ws_bytes = pkv.paged_attn_decode_workspace_size(
-        B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.max_blocks_per_seq, part)
+    ptok_fn = (pkv.paged_attn_decode_fp8_partition_tokens if fp8
+               else pkv.paged_attn_decode_partition_tokens)
+    ws_fn = (pkv.paged_attn_decode_fp8_workspace_size if fp8
+             else pkv.paged_attn_decode_workspace_size)
+    part = ptok_fn(B, w.num_q_heads, w.num_kv_heads, w.block_size, w.max_blocks_per_seq, part)
+    ws_bytes = ws_fn(B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                     w.max_blocks_per_seq, part)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
     has_pairs = "copy_pairs" in t
 

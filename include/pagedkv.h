@@ -267,7 +267,11 @@ int paged_attn_decode_shared_prefix(void* out, const void* q, const void* k_cach
  * q and out are `dtype` (PKV_BF16 or PKV_F16).  Codes convert exactly to fp16, so the
  * products run on the tensor cores in fp16 with fp32 accumulation.  head_dim must be 128
  * and block_size 16, 32 or 64.  Other arguments, the workspace and the return codes are
- * those of paged_attn_decode (the same workspace size).
+ * those of paged_attn_decode, except the default partition (partition_size 0): at one
+ * byte per element a token carries half the bytes, so the candidates double to 4096,
+ * 2048 and 1024 tokens (same 2048-work-unit rule).  The workspace is sized by
+ * paged_attn_decode_fp8_workspace_size (never more than paged_attn_decode_workspace_size
+ * for the same arguments).
  */
 int paged_attn_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
@@ -275,6 +279,18 @@ int paged_attn_decode_fp8(void* out, const void* q, const void* k_cache, const v
                           int max_blocks_per_seq, int num_blocks, float scale, float k_scale,
                           float v_scale, pkv_dtype dtype, int partition_size, void* workspace,
                           size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * Bytes of workspace paged_attn_decode_fp8 needs for these sizes (0 when no sequence can
+ * span more than one partition), and the partition size (tokens) it uses for this
+ * `partition_size` argument, or PKV_EINVAL.  Pure host functions; no CUDA call.
+ */
+size_t paged_attn_decode_fp8_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int block_size, int max_blocks_per_seq,
+                                            int partition_size);
+int paged_attn_decode_fp8_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads,
+                                           int block_size, int max_blocks_per_seq,
+                                           int partition_size);
 
 /*
  * kv_cache_write_fp8 -- kv_cache_write into E4M3 caches.

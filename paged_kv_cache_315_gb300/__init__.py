@@ -31,6 +31,8 @@ from ._binding import (  # noqa: F401
     load,
     paged_attn_decode,
     paged_attn_decode_fp8,
+    paged_attn_decode_fp8_partition_tokens,
+    paged_attn_decode_fp8_workspace_size,
     paged_attn_decode_noalloc,
     paged_attn_decode_partition_tokens,
     paged_attn_prefill,

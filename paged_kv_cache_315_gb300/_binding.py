@@ -58,6 +58,10 @@ def load() -> ctypes.CDLL:
         lib.paged_attn_decode_workspace_size.restype = sz
         lib.paged_attn_decode_partition_tokens.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.paged_attn_decode_partition_tokens.restype = i32
+        lib.paged_attn_decode_fp8_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        lib.paged_attn_decode_fp8_workspace_size.restype = sz
+        lib.paged_attn_decode_fp8_partition_tokens.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.paged_attn_decode_fp8_partition_tokens.restype = i32
         lib.paged_attn_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                                   i32, i32, f32, i32, i32, P]
         lib.paged_attn_decode_noalloc.restype = i32
@@ -160,6 +164,26 @@ def paged_attn_decode_partition_tokens(num_seqs: int, num_q_heads: int, num_kv_h
                                                         partition_size))
     if rc < 0:
         raise PagedKVError("paged_attn_decode_partition_tokens", rc)
+    return rc
+
+
+def paged_attn_decode_fp8_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                         head_dim: int, block_size: int,
+                                         max_blocks_per_seq: int,
+                                         partition_size: int = 0) -> int:
+    return int(load().paged_attn_decode_fp8_workspace_size(num_seqs, num_q_heads, num_kv_heads,
+                                                           head_dim, block_size,
+                                                           max_blocks_per_seq, partition_size))
+
+
+def paged_attn_decode_fp8_partition_tokens(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                           block_size: int, max_blocks_per_seq: int,
+                                           partition_size: int = 0) -> int:
+    rc = int(load().paged_attn_decode_fp8_partition_tokens(num_seqs, num_q_heads, num_kv_heads,
+                                                            block_size, max_blocks_per_seq,
+                                                            partition_size))
+    if rc < 0:
+        raise PagedKVError("paged_attn_decode_fp8_partition_tokens", rc)
     return rc
 
 
@@ -424,7 +448,7 @@ def paged_attn_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Ten
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("block_tables and context_lens must be int32")
     MB = block_tables.shape[1]
-    need = paged_attn_decode_workspace_size(B, Hq, Hkv, D, bs, MB, partition_size)
+    need = paged_attn_decode_fp8_workspace_size(B, Hq, Hkv, D, bs, MB, partition_size)
     if workspace is None:
         workspace = workspace_for(q.device, need, stream)
     ws_ptr = _cuda("workspace", workspace) if workspace is not None else None

@@ -117,7 +117,7 @@ int paged_attn_decode_fp8(void* out, const void* q, const void* k_cache, const v
   if (static_cast<long long>(num_blocks) * block_size >= INT_MAX) return PKV_EINVAL;
   if (static_cast<long long>(max_blocks_per_seq) * block_size >= INT_MAX) return PKV_EINVAL;
   const int ptok = resolve_partition_tokens(partition_size, block_size, num_seqs, num_q_heads,
-                                            num_kv_heads, max_blocks_per_seq);
+                                            num_kv_heads, max_blocks_per_seq, 1);
   if (ptok < 0) return PKV_EINVAL;
   if (!decode_fp8_supported(dtype, head_dim, block_size)) return PKV_EUNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
@@ -175,6 +175,30 @@ int paged_attn_decode_partition_tokens(int num_seqs, int num_q_heads, int num_kv
     return PKV_EINVAL;
   const int ptok = resolve_partition_tokens(partition_size, block_size, num_seqs, num_q_heads,
                                             num_kv_heads, max_blocks_per_seq);
+  return ptok < 0 ? PKV_EINVAL : ptok;
+}
+
+size_t paged_attn_decode_fp8_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                            int head_dim, int block_size, int max_blocks_per_seq,
+                                            int partition_size) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0)
+    return 0;
+  const int ptok = resolve_partition_tokens(partition_size, block_size, num_seqs, num_q_heads,
+                                            num_kv_heads, max_blocks_per_seq, 1);
+  if (ptok < 0) return 0;
+  return workspace_layout(num_seqs, num_q_heads, head_dim, block_size, max_blocks_per_seq, ptok)
+      .total;
+}
+
+int paged_attn_decode_fp8_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads,
+                                           int block_size, int max_blocks_per_seq,
+                                           int partition_size) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0)
+    return PKV_EINVAL;
+  const int ptok = resolve_partition_tokens(partition_size, block_size, num_seqs, num_q_heads,
+                                            num_kv_heads, max_blocks_per_seq, 1);
   return ptok < 0 ? PKV_EINVAL : ptok;
 }
 

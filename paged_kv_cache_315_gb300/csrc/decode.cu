@@ -195,6 +195,40 @@ __device__ __forceinline__ void issue_tile(const Params& P, const Smem& sm, cons
   }
 }
 
+// Stage and barrier phase of a warp's staged tiles.  Tile v sits in stage v % stages and
+// completes phase (v / stages) & 1 of that stage's barrier.  A warp visits tiles v,
+// v + kWarps, v + 2 kWarps, ... and the stage count is a multiple of kWarps, so both
+// advance without a division.
+struct StageCursor {
+  int st, ph;
+  __device__ __forceinline__ StageCursor(int v, int stages)
+      : st(v % stages), ph((v / stages) & 1) {}
+  __device__ __forceinline__ void next(int stages) {
+    st += kWarps;
+    if (st >= stages) {
+      st -= stages;
+      ph ^= 1;
+    }
+  }
+};
+
+// issue_tile for one physical block per stage (pair 1) with BOXES boxes per row segment,
+// into stage `st` (the stage of the tile it replaces); `y` is the block's TMA row.
+template <int BOXES>
+__device__ __forceinline__ void issue_block(const Params& P, const Smem& sm,
+                                            const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                            int st, int y, int x0) {
+  const uint32_t bar = smem_addr(&sm.bars[st]);
+  const uint32_t kdst = smem_addr(sm.ring + st * P.stage_bytes);
+  const uint32_t vdst = kdst + P.tile_stride;
+  mbar_arrive_expect_tx(bar, 2u * P.tile_bytes);
+#pragma unroll
+  for (int b = 0; b < BOXES; ++b) {
+    tma_load_2d(kdst + b * P.box_bytes, kmap, bar, x0 + b * P.box_cols, y);
+    tma_load_2d(vdst + b * P.box_bytes, vmap, bar, x0 + b * P.box_cols, y);
+  }
+}
+
 __device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, const Smem& sm,
                                                const CUtensorMap* kmap, const CUtensorMap* vmap,
                                                int x0, int spec_id) {
@@ -435,9 +469,11 @@ __global__ void __launch_bounds__(kThreads)
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
     const int je = min(w.nblk, (k + 1) * P.partition_blocks);
-    for (int j = k * P.partition_blocks + warp; j < je && !dead; j += kWarps) {
-      const int st = j % P.stages;
-      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (j / P.stages) & 1)) {
+    StageCursor cur(k * P.partition_blocks + warp, P.stages);
+    for (int j = k * P.partition_blocks + warp; j < je && !dead;
+         j += kWarps, cur.next(P.stages)) {
+      const int st = cur.st;
+      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), cur.ph)) {
         if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
         drain_after_timeout(P, w, sm, j);
         dead = true;
@@ -453,7 +489,8 @@ __global__ void __launch_bounds__(kThreads)
       }
       tc_block<T, D, BS>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
       __syncwarp();
-      if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0, w.nblk);
+      if (lane == 0 && j + P.stages < w.nblk)
+        issue_block<D / 64>(P, sm, &kmap, &vmap, st, sm.ycoord[j + P.stages], x0);
     }
 
     __syncthreads();  // every warp is done with partition k (and, with one partition, the ring)
@@ -604,9 +641,10 @@ __global__ void __launch_bounds__(kThreads)
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
     const int ve = min(nv, (k + 1) * vpp);
-    for (int v = k * vpp + warp; v < ve && !dead; v += kWarps) {
-      const int st = v % P.stages;
-      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (v / P.stages) & 1)) {
+    StageCursor cur(k * vpp + warp, P.stages);
+    for (int v = k * vpp + warp; v < ve && !dead; v += kWarps, cur.next(P.stages)) {
+      const int st = cur.st;
+      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), cur.ph)) {
         if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
         drain_after_timeout(P, w, sm, v);
         dead = true;
@@ -622,7 +660,12 @@ __global__ void __launch_bounds__(kThreads)
       }
       fp8_block<TR>(smem_addr(ktile), smem_addr(vtile), qa, o, m, l, valid, P.scale_log2, lane);
       __syncwarp();
-      if (lane == 0 && v + P.stages < nv) issue_tile(P, sm, &kmap, &vmap, v + P.stages, x0, w.nblk);
+      if (lane == 0 && v + P.stages < nv) {
+        if constexpr (PAIR == 1)
+          issue_block<1>(P, sm, &kmap, &vmap, st, sm.ycoord[v + P.stages], x0);
+        else
+          issue_tile(P, sm, &kmap, &vmap, v + P.stages, x0, w.nblk);
+      }
     }
 
     __syncthreads();
@@ -951,9 +994,11 @@ __global__ void __launch_bounds__(kThreads, 5)
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
     const int je = min(w.nblk, (k + 1) * P.partition_blocks);
-    for (int j = k * P.partition_blocks + warp; j < je && !dead; j += kWarps) {
-      const int st = j % P.stages;
-      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (j / P.stages) & 1)) {
+    StageCursor cur(k * P.partition_blocks + warp, P.stages);
+    for (int j = k * P.partition_blocks + warp; j < je && !dead;
+         j += kWarps, cur.next(P.stages)) {
+      const int st = cur.st;
+      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), cur.ph)) {
         if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
         drain_after_timeout(P, w, sm, j);
         dead = true;
@@ -969,7 +1014,8 @@ __global__ void __launch_bounds__(kThreads, 5)
       }
       tcg_block<T, BS>(smem_addr(ktile), smem_addr(vtile), qb, o, m, l, valid, P.scale_log2, lane);
       __syncwarp();
-      if (lane == 0 && j + P.stages < w.nblk) issue_tile(P, sm, &kmap, &vmap, j + P.stages, x0, w.nblk);
+      if (lane == 0 && j + P.stages < w.nblk)
+        issue_block<2>(P, sm, &kmap, &vmap, st, sm.ycoord[j + P.stages], x0);
     }
 
     __syncthreads();
@@ -1172,9 +1218,10 @@ __global__ void __launch_bounds__(kThreads, 5)
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
     const int ve = min(nv, (k + 1) * vpp);
-    for (int v = k * vpp + warp; v < ve && !dead; v += kWarps) {
-      const int st = v % P.stages;
-      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), (v / P.stages) & 1)) {
+    StageCursor cur(k * vpp + warp, P.stages);
+    for (int v = k * vpp + warp; v < ve && !dead; v += kWarps, cur.next(P.stages)) {
+      const int st = cur.st;
+      if (!mbar_wait_bounded(smem_addr(&sm.bars[st]), cur.ph)) {
         if (lane == 0) raise_error(P.err, PKV_DERR_TIMEOUT);
         drain_after_timeout(P, w, sm, v);
         dead = true;
@@ -1190,7 +1237,12 @@ __global__ void __launch_bounds__(kThreads, 5)
       }
       fp8g_block<TR>(smem_addr(ktile), smem_addr(vtile), qb, o, m, l, valid, P.scale_log2, lane);
       __syncwarp();
-      if (lane == 0 && v + P.stages < nv) issue_tile(P, sm, &kmap, &vmap, v + P.stages, x0, w.nblk);
+      if (lane == 0 && v + P.stages < nv) {
+        if constexpr (PAIR == 1)
+          issue_block<1>(P, sm, &kmap, &vmap, st, sm.ycoord[v + P.stages], x0);
+        else
+          issue_tile(P, sm, &kmap, &vmap, v + P.stages, x0, w.nblk);
+      }
     }
 
     __syncthreads();
@@ -1473,20 +1525,22 @@ constexpr int kMaxSmem = 227 * 1024;
 size_t dtype_size(pkv_dtype dtype) { return dtype == PKV_F32 ? 4 : 2; }
 
 int resolve_partition_tokens(int partition_size, int block_size, int num_seqs, int num_q_heads,
-                             int num_kv_heads, int max_blocks_per_seq) {
+                             int num_kv_heads, int max_blocks_per_seq, int kv_elem_bytes) {
   if (block_size <= 0) return -1;
   if (partition_size == 0) {
-    // The largest of 2048, 1024, 512 tokens that still leaves at least kMinUnits work
-    // units (sequence x KV head x 16-head chunk x partition, counting every sequence at
-    // the block table's full length); longer partitions amortise each CTA's start-up
-    // cost, shorter ones balance uneven contexts across the SMs.
+    // The largest of 2048, 1024, 512 tokens (x2 for 1-byte E4M3 elements, so a work unit
+    // carries the same bytes) that still leaves at least kMinUnits work units (sequence x
+    // KV head x 16-head chunk x partition, counting every sequence at the block table's
+    // full length); longer partitions amortise each CTA's start-up cost, shorter ones
+    // balance uneven contexts across the SMs.
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
     const int group = num_kv_heads > 0 ? std::max(1, num_q_heads / num_kv_heads) : 1;
     const long long heads = static_cast<long long>(std::max(0, num_seqs)) *
                             std::max(1, num_kv_heads) * ((group + kTcHeads - 1) / kTcHeads);
+    const int widen = kv_elem_bytes == 1 ? 2 : 1;
     int t = 0;
     for (int cand : {2048, 1024, kDefaultPartitionTokens}) {
-      t = std::max(block_size, (cand / block_size) * block_size);
+      t = std::max(block_size, (widen * cand / block_size) * block_size);
       if (heads * ((max_ctx + t - 1) / t) >= kMinUnits) break;
     }
     return t;

@@ -36,9 +36,10 @@ struct DecodeArgs {
 };
 
 // Resolved partition size in tokens, or -1 if `partition_size` is not acceptable.
-// 0 selects a default from the batch's shape (pure host arithmetic).
+// 0 selects a default from the batch's shape and the cache's bytes per element
+// (`kv_elem_bytes`: 2 for 16-bit caches, 1 for E4M3; pure host arithmetic).
 int resolve_partition_tokens(int partition_size, int block_size, int num_seqs, int num_q_heads,
-                             int num_kv_heads, int max_blocks_per_seq);
+                             int num_kv_heads, int max_blocks_per_seq, int kv_elem_bytes = 2);
 
 // Workspace layout shared by the size query and the launcher.
 struct WorkspaceLayout {

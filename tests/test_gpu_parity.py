@@ -625,9 +625,10 @@ def test_fp8_full_size_benchmark_batches(pkv, cfg):
     pkv.kv_cache_write_fp8(t["k_new"], t["v_new"], t["k8"], t["v8"], t["slot_mapping"], ks, vs)
     assert oracle.kv_cache_write_fp8(w.k_new, w.v_new, k8, v8, w.slot_mapping, ks, vs,
                                      "bf16") == 0
-    part = pkv.paged_attn_decode_partition_tokens(w.num_seqs, w.num_q_heads, w.num_kv_heads,
-                                                  w.block_size, w.max_blocks_per_seq,
-                                                  w.partition_size)
+    # the partition size bench.py launches E4M3 decode with
+    part = pkv.paged_attn_decode_fp8_partition_tokens(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                      w.block_size, w.max_blocks_per_seq,
+                                                      w.partition_size)
     out = torch.empty_like(t["q"])
     pkv.paged_attn_decode_fp8(out, t["q"], t["k8"], t["v8"], t["block_tables"], t["context_lens"],
                               w.scale, ks, vs, partition_size=part)
