@@ -312,6 +312,23 @@ __device__ __forceinline__ uint32_t swz(int r, int d) {
   return static_cast<uint32_t>((d >> 6) * (BS * 128) + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4));
 }
 
+// The same offsets for the ldmatrix pattern of an m16n8k16 A operand, split into a lane
+// part and a step part.  Lane `lane` reads row (lane & 7) + 8 * bit `rbit` of the lane and
+// 16-byte chunk 2 s + bit `cbit` of K-step s (s = 0..7, 8 columns per chunk); with the
+// tile base 1024-byte aligned,
+//     base + swz<BS>(16 t + row, 16 s + 8 cbit) = ((base + lane_off) ^ ((s & 3) << 5))
+//                                                 + (s >> 2) * BS * 128 + 2048 t,
+// since the step only flips chunk bits 1-2 (byte bits 5-6) of a 1024-byte-aligned row group.
+__device__ __forceinline__ uint32_t ldsm_lane_off(int lane, int rbit, int cbit) {
+  const int row = (lane & 7) + ((lane >> rbit) & 1) * 8;
+  return static_cast<uint32_t>(row * 128 + ((((lane >> cbit) & 1) ^ (lane & 7)) << 4));
+}
+template <int BS>
+__device__ __forceinline__ uint32_t ldsm_step(uint32_t base_lane, int s, int t) {
+  return (base_lane ^ static_cast<uint32_t>((s & 3) << 5)) +
+         static_cast<uint32_t>((s >> 2) * (BS * 128) + 2048 * t);
+}
+
 // One block's online-softmax step on the S fragments of an m16n8 tile row pair: scale into
 // log2 units, mask tokens past `valid`, update the running max m and sum l (rows lane/4
 // and lane/4 + 8), rescale the output accumulators, and return P = 2^(S - m) rounded to
@@ -879,22 +896,24 @@ KernelFn simt_kernel_for(int D) {
 // enters as the A operand through ldmatrix, V^T through ldmatrix.trans, and P^T through two
 // movmatrix transposes per 16 tokens; Q^T's B fragments stay in registers.  Half the
 // accumulator and Q registers of the M = heads layout, so more CTAs fit on an SM.
+// kl, vl: ldsm_lane_off(lane, 3, 4) and ldsm_lane_off(lane, 4, 3), computed once per CTA.
 template <typename T, int BS>
-__device__ __forceinline__ void tcg_block(uint32_t kb, uint32_t vb, const uint32_t (&qb)[8][2],
-                                          float (&o)[8][4], float (&m)[2], float (&l)[2],
-                                          int valid, float scale_log2, int lane) {
+__device__ __forceinline__ void tcg_block(uint32_t kb, uint32_t vb, uint32_t kl, uint32_t vl,
+                                          const uint32_t (&qb)[8][2], float (&o)[8][4],
+                                          float (&m)[2], float (&l)[2], int valid,
+                                          float scale_log2, int lane) {
   constexpr int MT = BS / 16;
   const int r8 = lane >> 2;
   float sc[MT][4];
+  // A fragment rows: token mt*16 + (lane & 7) + 8 * ((lane >> 3) & 1), cols +8 for lanes 16-31
+  const uint32_t kbl = kb + kl;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
-    // A fragment rows: token mt*16 + (lane & 7) + 8 * ((lane >> 3) & 1), cols +8 for lanes 16-31
-    const int r = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t a[4];
-      ldsm_x4(kb + swz<BS>(r, kk * 16 + (lane >> 4) * 8), a[0], a[1], a[2], a[3]);
+      ldsm_x4(ldsm_step<BS>(kbl, kk, mt), a[0], a[1], a[2], a[3]);
       Mma<T>::run(sc[mt], a, qb[kk][0], qb[kk][1]);
     }
   }
@@ -946,13 +965,14 @@ __device__ __forceinline__ void tcg_block(uint32_t kb, uint32_t vb, const uint32
   l[0] += rs0;
   l[1] += rs1;
   // O^T += V^T . P^T: A fragments of V^T (rows d, cols tokens) by transposing loads of V
+  // rows kt*16 + (lane & 7) + 8 * ((lane >> 4) & 1), cols +8 for lanes 8-15 and 24-31
+  const uint32_t vbl = vb + vl;
 #pragma unroll
   for (int kt = 0; kt < MT; ++kt) {
-    const int r = kt * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
 #pragma unroll
     for (int md = 0; md < 8; ++md) {
       uint32_t a[4];
-      ldsm_x4_trans(vb + swz<BS>(r, md * 16 + ((lane >> 3) & 1) * 8), a[0], a[1], a[2], a[3]);
+      ldsm_x4_trans(ldsm_step<BS>(vbl, md, kt), a[0], a[1], a[2], a[3]);
       Mma<T>::run(o[md], a, pb[kt][0], pb[kt][1]);
     }
   }
@@ -971,6 +991,7 @@ __global__ void __launch_bounds__(kThreads, 5)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int x0 = w.g * D;
   pipeline_start(P, w, sm, &kmap, &vmap, x0, spec_id);
+  const uint32_t kl = ldsm_lane_off(lane, 3, 4), vl = ldsm_lane_off(lane, 4, 3);
 
   // Q^T B fragments: head r8, head_dim kk*16 + 2c (+1) and kk*16 + 8 + 2c (+1)
   uint32_t qb[8][2];
@@ -1012,7 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 5)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      tcg_block<T, BS>(smem_addr(ktile), smem_addr(vtile), qb, o, m, l, valid, P.scale_log2, lane);
+      tcg_block<T, BS>(smem_addr(ktile), smem_addr(vtile), kl, vl, qb, o, m, l, valid,
+                       P.scale_log2, lane);
       __syncwarp();
       if (lane == 0 && j + P.stages < w.nblk)
         issue_block<2>(P, sm, &kmap, &vmap, st, sm.ycoord[j + P.stages], x0);
