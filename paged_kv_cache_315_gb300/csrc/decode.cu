@@ -169,7 +169,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const Params& P) {
 
 // Resolve the partition's block ids to TMA row coordinates (invalid ids point past the
 // tensor, so their tiles load as zeros), initialise the stage barriers and issue the
-// first S tile loads.
+// first S tile loads.  Called by every thread of the CTA.
 __device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, const Smem& sm,
                                                const CUtensorMap* kmap, const CUtensorMap* vmap,
                                                int x0, int spec_id);
@@ -232,27 +232,36 @@ __device__ __forceinline__ void issue_block(const Params& P, const Smem& sm,
 __device__ __forceinline__ void pipeline_start(const Params& P, const Work& w, const Smem& sm,
                                                const CUtensorMap* kmap, const CUtensorMap* vmap,
                                                int x0, int spec_id) {
-  const int tid = threadIdx.x;
-  const int32_t* bt = P.block_tables + static_cast<size_t>(w.s) * P.max_blocks_per_seq + w.blk0;
-  for (int j = tid; j < w.nblk; j += kThreads) {
-    int id = j == tid ? spec_id : bt[j];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto row_of = [&](int id) {
     if (id < 0 || id >= P.num_blocks) {
       raise_error(P.err, PKV_DERR_BLOCK_ID);
       id = P.num_blocks;
     }
-    sm.ycoord[j] = id * P.block_size;
-  }
+    return id * P.block_size;
+  };
+  // the first kThreads ids were loaded by decode_work (one per thread)
+  if (tid < w.nblk) sm.ycoord[tid] = row_of(spec_id);
   if (tid == 0) {
+    tma_prefetch_desc(kmap);
+    tma_prefetch_desc(vmap);
     for (int i = 0; i < P.stages; ++i) mbar_init(smem_addr(&sm.bars[i]), 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
-    tma_prefetch_desc(kmap);
-    tma_prefetch_desc(vmap);
+  // Each warp issues the first tiles of its own stages (tile v: stage v, owner warp v % 4);
+  // they need at most stages * pair ids, all among the first kThreads.
+  static_assert(kWarps * kMaxStageSet * 2 <= kThreads, "first tiles' ids come from decode_work");
+  if (lane == 0) {
     const int nv = (w.nblk + P.pair - 1) / P.pair;
     const int first = min(P.stages, nv);
-    for (int v = 0; v < first; ++v) issue_tile(P, sm, kmap, vmap, v, x0, w.nblk);
+    for (int v = warp; v < first; v += kWarps) issue_tile(P, sm, kmap, vmap, v, x0, w.nblk);
+  }
+  // ids past the first kThreads: loaded while the first tiles are in flight
+  if (w.nblk > kThreads) {
+    const int32_t* bt = P.block_tables + static_cast<size_t>(w.s) * P.max_blocks_per_seq + w.blk0;
+    for (int j = tid + kThreads; j < w.nblk; j += kThreads) sm.ycoord[j] = row_of(bt[j]);
+    __syncthreads();
   }
 }
 
