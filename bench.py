@@ -50,15 +50,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each (the
     # timed step of `bench.py --steps 1 --warmup 3`)
-    "13b-mha-b64-bf16@2048": {"bytes": 1408769792 + 668672, "decode_cu_sha": "b160b5674f9dae30"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963336192 + 3542016, "decode_cu_sha": "b160b5674f9dae30"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328343040 + 2344960, "decode_cu_sha": "b160b5674f9dae30"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4296091136 + 37296640, "decode_cu_sha": "b160b5674f9dae30"},
-    "13b-mha-b64-bf16@2048+fp8": {"bytes": 704751872 + 625664, "decode_cu_sha": "b160b5674f9dae30"},
-    "70b-gqa8-b128-bf16@2048+fp8": {"bytes": 483123712 + 2494208, "decode_cu_sha": "b160b5674f9dae30"},
-    "shared-prefix-cow-b256-bf16@2048+fp8": {"bytes": 164948992 + 2191616, "decode_cu_sha": "b160b5674f9dae30"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148129792 + 31825664, "decode_cu_sha": "b160b5674f9dae30"},
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1992766720 + 25097472, "decode_cu_sha": "b160b5674f9dae30"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408769536 + 628480, "decode_cu_sha": "9ac65a69fd446365"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963327232 + 3317248, "decode_cu_sha": "9ac65a69fd446365"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328334080 + 1528576, "decode_cu_sha": "9ac65a69fd446365"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4296169472 + 37059840, "decode_cu_sha": "9ac65a69fd446365"},
+    "13b-mha-b64-bf16@4096+fp8": {"bytes": 704796416 + 2790656, "decode_cu_sha": "9ac65a69fd446365"},
+    "70b-gqa8-b128-bf16@4096+fp8": {"bytes": 482520064 + 2760192, "decode_cu_sha": "9ac65a69fd446365"},
+    "shared-prefix-cow-b256-bf16@4096+fp8": {"bytes": 164961024 + 1602304, "decode_cu_sha": "9ac65a69fd446365"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2151094272 + 39941888, "decode_cu_sha": "9ac65a69fd446365"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 2052940544 + 24969984, "decode_cu_sha": "9ac65a69fd446365"},
 }
 
 
@@ -245,8 +245,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393143040, "sources_sha": "e1d88619f3faa3db"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 354289152, "sources_sha": "e1d88619f3faa3db"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393668608, "sources_sha": "5427c38343b4459e"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353544704, "sources_sha": "5427c38343b4459e"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 
@@ -941,10 +941,10 @@ def run_swap(args) -> None:
 # batches (head_dim 128 and 64), from one ncu capture each, valid only for the kernel source
 # whose hash is recorded.
 PREFILL_TRAFFIC = {
-    "chunked-prefill-70b-gqa8-c512": {"bytes": 278784256 + 103175424,
-                                      "prefill_cu_sha": "cad756ccb9424f88"},
-    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139377664 + 36586496,
-                                          "prefill_cu_sha": "cad756ccb9424f88"},
+    "chunked-prefill-70b-gqa8-c512": {"bytes": 278722048 + 103225600,
+                                      "prefill_cu_sha": "a81684fcdb4147ba"},
+    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139449088 + 36960256,
+                                          "prefill_cu_sha": "a81684fcdb4147ba"},
 }
 
 
