@@ -72,6 +72,7 @@ struct Params {
   int merge_off;    // byte offset of the merge buffer from the ring (0: the ring itself)
   const int32_t* order;  // CTA work order over (sequence, partition group) items, or null
   int force_partials;    // every context leaves (m, l, o) partials, none writes `out`
+  int fold;              // a CTA folds its ppc partitions into one partial (see finish_part)
   float scale_log2;
   float out_scale;  // multiplies every output (the V scale of fp8 caches, else 1)
 };
@@ -305,6 +306,82 @@ __device__ void finish(const Params& P, const Work& w, int D, int HC, const floa
       if (d == 0) {
         P.ws_ml[idx * 2] = M;
         P.ws_ml[idx * 2 + 1] = den;
+      }
+    }
+  }
+}
+
+// Partition k of the CTA's group (partitions w.p .. w.p + w.nparts - 1).  Unless the launch
+// folds (P.fold: ppc > 1 and no per-partition partials wanted; FOLD = false compiles the
+// kernel without this path), this is finish().  Folding, the CTA combines its partitions
+// into one (m, l, o) by log-sum-exp as it goes, keeping the running value in the group's
+// partial slot w.p / ppc (read back by the same threads), and after the last partition
+// writes either the output (the group covers the whole context) or that one partial for
+// decode_merge_kernel.  Called by every thread.
+template <typename T, bool FOLD>
+__device__ void finish_part(const Params& P, const Work& w, int k, int D, int HC,
+                            const float* O_s, const float* ml_s) {
+  if (!FOLD || !P.fold) {
+    Work wk = w;
+    wk.p = w.p + k;
+    finish<T>(P, wk, D, HC, O_s, ml_s);
+    return;
+  }
+  constexpr int kMaxPer = 4;  // elements per thread: head_chunk * D <= 4 * kThreads
+  const int tid = threadIdx.x;
+  const int n = w.hc * D;
+  const int groups = (w.np + P.ppc - 1) / P.ppc;
+  const bool last = k == w.nparts - 1;
+  const size_t slot = static_cast<size_t>(w.p / P.ppc);
+  float Ms[kMaxPer], Ds[kMaxPer], Ns[kMaxPer];
+#pragma unroll
+  for (int q = 0; q < kMaxPer; ++q) {
+    const int i = tid + q * kThreads;
+    if (i >= n) break;
+    const int r = i / D, d = i - r * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int wi = 0; wi < kWarps; ++wi) M = fmaxf(M, ml_s[(wi * HC + r) * 2]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < kWarps; ++wi) {
+      const float mw = ml_s[(wi * HC + r) * 2];
+      const float cw = mw == -INFINITY ? 0.f : exp2f(mw - M);
+      num += cw * O_s[(wi * HC + r) * D + d];
+      den += cw * ml_s[(wi * HC + r) * 2 + 1];
+    }
+    if (k > 0) {
+      // fold in the running value of the partitions before this one
+      const size_t idx = (static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r) * P.max_parts + slot;
+      const float Mp = P.ws_ml[idx * 2], Dp = P.ws_ml[idx * 2 + 1], Np = P.ws_o[idx * D + d];
+      const float Mn = fmaxf(M, Mp);
+      const float a = Mp == -INFINITY ? 0.f : exp2f(Mp - Mn);
+      const float b = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      num = Np * a + num * b;
+      den = Dp * a + den * b;
+      M = Mn;
+    }
+    Ms[q] = M;
+    Ds[q] = den;
+    Ns[q] = num;
+  }
+  // every thread has read the running (m, l) of its rows before any thread rewrites them
+  if (k > 0) __syncthreads();
+  T* out = static_cast<T*>(P.out);
+#pragma unroll
+  for (int q = 0; q < kMaxPer; ++q) {
+    const int i = tid + q * kThreads;
+    if (i >= n) break;
+    const int r = i / D, d = i - r * D;
+    const size_t row = static_cast<size_t>(w.s) * P.num_q_heads + w.h0 + r;
+    if (last && groups <= 1) {
+      out[row * D + d] = from_f32<T>(Ns[q] / Ds[q] * P.out_scale);
+    } else {
+      const size_t idx = row * P.max_parts + slot;
+      P.ws_o[idx * D + d] = Ns[q];
+      if (d == 0) {
+        P.ws_ml[idx * 2] = Ms[q];
+        P.ws_ml[idx * 2 + 1] = Ds[q];
       }
     }
   }
@@ -550,9 +627,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     __syncthreads();
-    Work wk = w;
-    wk.p = w.p + k;
-    finish<T>(P, wk, D, HC, O_s, ml_s);
+    finish_part<T, BS == 16>(P, w, k, D, HC, O_s, ml_s);
     if (k + 1 < w.nparts) __syncthreads();  // the merge buffer is read before it is reused
   }
 }
@@ -725,9 +800,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     __syncthreads();
-    Work wk = w;
-    wk.p = w.p + k;
-    finish<T>(P, wk, D, HC, O_s, ml_s);
+    finish_part<T, false>(P, w, k, D, HC, O_s, ml_s);
     if (k + 1 < w.nparts) __syncthreads();
   }
 }
@@ -1085,9 +1158,7 @@ __global__ void __launch_bounds__(kThreads, 5)
       }
     }
     __syncthreads();
-    Work wk = w;
-    wk.p = w.p + k;
-    finish<T>(P, wk, D, HC, O_s, ml_s);
+    finish_part<T, BS == 16>(P, w, k, D, HC, O_s, ml_s);
     if (k + 1 < w.nparts) __syncthreads();
   }
 }
@@ -1312,9 +1383,7 @@ __global__ void __launch_bounds__(kThreads, 5)
       }
     }
     __syncthreads();
-    Work wk = w;
-    wk.p = w.p + k;
-    finish<T>(P, wk, D, HC, O_s, ml_s);
+    finish_part<T, false>(P, w, k, D, HC, O_s, ml_s);
     if (k + 1 < w.nparts) __syncthreads();
   }
 }
@@ -1443,8 +1512,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
     int L = P.context_lens[row / P.num_q_heads];
     const int Lmax = P.max_blocks_per_seq * P.block_size;
     L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
-    const int ptok = P.partition_blocks * P.block_size;
-    np = (L + ptok - 1) / ptok;
+    // one partial per partition, or per group of ppc partitions when the CTAs fold them
+    const int gtok = P.partition_blocks * P.block_size * (P.fold ? P.ppc : 1);
+    np = (L + gtok - 1) / gtok;
   }
   // every thread waits, even one with nothing to merge, so that this grid never ends
   // before the decode grid it depends on
@@ -1661,6 +1731,8 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   // Short partitions on the tensor-core paths: a CTA streams two of them back to back
   // (one partial each) when its merge buffer still lets three CTAs share an SM.
   P.ppc = 1;
+  // (a CTA's group of partitions is folded by threads holding at most 4 elements each:
+  // head_chunk * D <= 4 * kThreads)
   if (tc && a.partition_tokens < 1024 && P.head_chunk <= 4 && wl.max_parts > 1 &&
       P.partition_blocks % (4 * P.pair) == 0) {
     const Geometry g2 = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
@@ -1668,6 +1740,10 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     if ((shallow ? 5 : 3) * (g2.smem_bytes + 1024) <= 228 * 1024) P.ppc = 2;
   }
   P.max_groups = (wl.max_parts + P.ppc - 1) / P.ppc;
+  // the 16-bit kernels of 16-token blocks fold a CTA's partitions into one partial (their
+  // instantiation has the code for it); the others, at the edge of their register budgets,
+  // leave one per partition
+  P.fold = P.ppc > 1 && !a.partials_out && !a.kv_fp8 && BS == 16 ? 1 : 0;
   const Geometry g = geometry(a.dtype, D, BS, tc, P.partition_blocks, wl.max_parts, a.kv_fp8,
                               P.pair, P.ppc, P.head_chunk, shallow);
   P.merge_off = g.merge_off;
