@@ -166,8 +166,11 @@ def test_decode_matches_oracle(pkv, dtype, Hq, Hkv, D, bs, part):
 
 
 # Partitions of at most 512 tokens with at most 4 query heads per KV head: one CTA streams
-# two consecutive partitions and writes a partial for each.  Lengths end on, before and
-# after partition edges so that CTAs see one or two live partitions and ragged tails.
+# two consecutive partitions.  With 16-token blocks (bf16, f16) it folds them into one
+# partial, or writes the output when they cover the whole context; otherwise it writes a
+# partial for each.  Lengths end on, before and after partition edges so that CTAs see one
+# or two live partitions, groups that cover the whole context, odd partition counts and
+# ragged tails.
 PAIRED_LENS = [1, 511, 512, 513, 1024, 1025, 1543, 2048, 2660, 0, 3000, 257]
 
 
