@@ -81,7 +81,8 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
 // 3-D TMA box per 64 columns (G heads x 128/G tokens); with any other G, and for a negative
 // scale, each softmax thread stages its own query row instead (QT), with its signs flipped
 // for a negative scale.
-// Tensor memory (256 columns): two 64-column score buffers and the 128-column output.
+// Tensor memory (256 columns): two 64-column score buffers and the 128-column output (at
+// head_dim 64: three score buffers and a 64-column output).
 //   S_b = Q . K_j^T       (M 128, N 64, K 128; A and B K-major from shared memory)
 //   P_j                   (bf16, written over the first 32 columns of S_b)
 //   O  += P_j . V_j       (M 128, N 128, K 64; A from tensor memory, V MN-major)
@@ -116,6 +117,9 @@ __global__ void __launch_bounds__(kUThreads, 2)
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
   constexpr uint32_t kIdQK = umma_idesc(kURows, kUKeys, kBf16, false);
   constexpr uint32_t kIdPV = umma_idesc(kURows, D, kBf16, true);
+  // score buffers: at head_dim 64 the output takes 64 columns, so a third 64-column buffer
+  // fits in the CTA's 256 (QK(j) then waits for PV(j - 3) instead of PV(j - 2))
+  constexpr int SB = D == 64 ? 3 : 2;
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -175,10 +179,10 @@ __global__ void __launch_bounds__(kUThreads, 2)
   uint64_t* k_empty = k_full + kUStages;         // [kUStages]
   uint64_t* v_full = k_empty + kUStages;         // [kUStages]
   uint64_t* v_empty = v_full + kUStages;         // [kUStages]
-  uint64_t* s_full = v_empty + kUStages;         // [2]
-  uint64_t* p_full = s_full + 2;                 // [2]
-  uint64_t* pv_done = p_full + 2;
-  uint64_t* drain = pv_done + 1;
+  uint64_t* s_full = v_empty + kUStages;         // [SB]
+  uint64_t* p_full = s_full + SB;                // [SB]
+  uint64_t* pv_done = p_full + SB;               // [SB]: the P.V of the tiles using S_b
+  uint64_t* drain = pv_done + SB;
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(drain + 1);
   // [0] abort, [1] K tiles issued, [2] V tiles issued
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_base + 1);
@@ -191,11 +195,11 @@ __global__ void __launch_bounds__(kUThreads, 2)
       mbar_init(smem_addr(&v_full[i]), 1);
       mbar_init(smem_addr(&v_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < SB; ++i) {
       mbar_init(smem_addr(&s_full[i]), 1);
       mbar_init(smem_addr(&p_full[i]), 4);
+      mbar_init(smem_addr(&pv_done[i]), 1);
     }
-    mbar_init(smem_addr(pv_done), 1);
     mbar_init(smem_addr(drain), 1);
     flags[0] = 0;
     flags[1] = 0;
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tm = *tmem_base;
-  const uint32_t tm_o = tm + 2 * kUKeys;
+  const uint32_t tm_o = tm + SB * kUKeys;
 
   auto fail = [&](void) {
     raise_error(P.err, PKV_DERR_TIMEOUT);
@@ -299,9 +303,9 @@ __global__ void __launch_bounds__(kUThreads, 2)
     if (!ok && lane == 0) fail();
     int issued_mma = 0;
     auto pv = [&](int i) -> bool {  // O += P_i . V_i
-      const int st = i % kUStages, b = i & 1;
+      const int st = i % kUStages, b = i % SB;
       int okp = 1;
-      if (lane == 0) okp = mbar_wait_bounded(smem_addr(&p_full[b]), (i >> 1) & 1) ? 1 : 0;
+      if (lane == 0) okp = mbar_wait_bounded(smem_addr(&p_full[b]), (i / SB) & 1) ? 1 : 0;
       okp = __shfl_sync(0xffffffffu, okp, 0);
       // every lane observes the V tile's arrival (the warp may zero part of it)
       const bool okv = okp && __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&v_full[st]),
@@ -336,7 +340,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
                        dv + static_cast<uint64_t>(kt * 128), kIdPV,
                        (i > 0 || kt > 0) ? 1u : 0u);
         umma_commit_warp(iss, smem_addr(&v_empty[st]));
-        umma_commit_warp(iss, smem_addr(pv_done));
+        umma_commit_warp(iss, smem_addr(&pv_done[b]));
       } else if (lane == 0) {
         tc_fence_after_sync();
 #pragma unroll
@@ -345,12 +349,12 @@ __global__ void __launch_bounds__(kUThreads, 2)
                   dv + static_cast<uint64_t>(kt * 128), kIdPV,
                   (i > 0 || kt > 0) ? 1u : 0u);
         umma_commit(smem_addr(&v_empty[st]));
-        umma_commit(smem_addr(pv_done));
+        umma_commit(smem_addr(&pv_done[b]));
       }
       return true;
     };
     for (int j = 0; ok && j < ntiles; ++j) {
-      const int st = j % kUStages, b = j & 1;
+      const int st = j % kUStages, b = j % SB;
       int okk = 1;
       if (lane == 0) okk = mbar_wait_bounded(smem_addr(&k_full[st]), (j / kUStages) & 1) ? 1 : 0;
       okk = __shfl_sync(0xffffffffu, okk, 0);
@@ -359,11 +363,11 @@ __global__ void __launch_bounds__(kUThreads, 2)
         ok = 0;
         break;
       }
-      // S_b still holds P_{j-2}: the P.V that reads it must be complete before QK(j)
-      // overwrites it
-      if (j >= 2) {
+      // S_b still holds P_{j-SB}: the P.V that reads it must be complete before QK(j)
+      // overwrites it (that P.V is the ((j - SB) / SB)-th completion of pv_done[b])
+      if (j >= SB) {
         int okv = 1;
-        if (lane == 0) okv = mbar_wait_bounded(smem_addr(pv_done), (j - 2) & 1) ? 1 : 0;
+        if (lane == 0) okv = mbar_wait_bounded(smem_addr(&pv_done[b]), ((j - SB) / SB) & 1) ? 1 : 0;
         okv = __shfl_sync(0xffffffffu, okv, 0);
         if (!okv) {
           if (lane == 0) fail();
@@ -440,10 +444,10 @@ __global__ void __launch_bounds__(kUThreads, 2)
     float m = -INFINITY, l = 0.f;
     int done = 0;
     for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
+      const int b = j % SB;
       // warp-uniform decisions: the tensor-memory accesses below are warp-collective
       if (__any_sync(0xffffffffu, flags[0] != 0)) break;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&s_full[b]), (j >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&s_full[b]), (j / SB) & 1))) {
         if (lane == 0) fail();
         break;
       }
@@ -514,7 +518,8 @@ __global__ void __launch_bounds__(kUThreads, 2)
       const float alpha = exp2f(m - mn);  // 0 on the first tile (m = -inf), 1 if m stays
       if (j > 0 && __any_sync(0xffffffffu, up)) {
         // O's rows move to the new reference: the previous P.V must have landed
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(pv_done), (j - 1) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&pv_done[(j - 1) % SB]),
+                                                        ((j - 1) / SB) & 1))) {
           if (lane == 0) fail();
           break;
         }
@@ -539,7 +544,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
       done = j + 1;
     }
     // the last P.V: waited on through `drain`, which the MMA thread commits after it (a
-    // parity wait on pv_done cannot tell PV(ntiles-1) from PV(ntiles-3))
+    // parity wait on pv_done[b] cannot tell PV(ntiles-1) from PV(ntiles-1-2SB))
     if (done == ntiles && !__any_sync(0xffffffffu, flags[0] != 0)) {
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(drain), 0))) {
         if (lane == 0) fail();
