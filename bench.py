@@ -50,15 +50,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each (the
     # timed step of `bench.py --steps 1 --warmup 3`)
-    "13b-mha-b64-bf16@2048": {"bytes": 1408769536 + 628480, "decode_cu_sha": "9ac65a69fd446365"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963327232 + 3317248, "decode_cu_sha": "9ac65a69fd446365"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328334080 + 1528576, "decode_cu_sha": "9ac65a69fd446365"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4296169472 + 37059840, "decode_cu_sha": "9ac65a69fd446365"},
-    "13b-mha-b64-bf16@4096+fp8": {"bytes": 704796416 + 2790656, "decode_cu_sha": "9ac65a69fd446365"},
-    "70b-gqa8-b128-bf16@4096+fp8": {"bytes": 482520064 + 2760192, "decode_cu_sha": "9ac65a69fd446365"},
-    "shared-prefix-cow-b256-bf16@4096+fp8": {"bytes": 164961024 + 1602304, "decode_cu_sha": "9ac65a69fd446365"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2151094272 + 39941888, "decode_cu_sha": "9ac65a69fd446365"},
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 2052940544 + 24969984, "decode_cu_sha": "9ac65a69fd446365"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408782592 + 623360, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963332096 + 2517504, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328232960 + 1576704, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4300963840 + 32441344, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "13b-mha-b64-bf16@4096+fp8": {"bytes": 704823296 + 2732800, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "70b-gqa8-b128-bf16@4096+fp8": {"bytes": 482562560 + 2753280, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "shared-prefix-cow-b256-bf16@4096+fp8": {"bytes": 164957696 + 1674240, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2151155968 + 40330752, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1968898048 + 20549888, "decode_cu_sha": "9560b5ee8e925ceb"},
 }
 
 
@@ -245,8 +245,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393668608, "sources_sha": "5427c38343b4459e"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353544704, "sources_sha": "5427c38343b4459e"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1392898816, "sources_sha": "5a92943affb3de81"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353465600, "sources_sha": "5a92943affb3de81"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 
@@ -941,10 +941,10 @@ def run_swap(args) -> None:
 # batches (head_dim 128 and 64), from one ncu capture each, valid only for the kernel source
 # whose hash is recorded.
 PREFILL_TRAFFIC = {
-    "chunked-prefill-70b-gqa8-c512": {"bytes": 278722048 + 103225600,
-                                      "prefill_cu_sha": "a81684fcdb4147ba"},
-    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139449088 + 36960256,
-                                          "prefill_cu_sha": "a81684fcdb4147ba"},
+    "chunked-prefill-70b-gqa8-c512": {"bytes": 278717184 + 103227648,
+                                      "prefill_cu_sha": "5f787fdc73ef55bb"},
+    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139378432 + 36558080,
+                                          "prefill_cu_sha": "5f787fdc73ef55bb"},
 }
 
 
