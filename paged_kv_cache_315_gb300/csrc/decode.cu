@@ -1181,9 +1181,12 @@ KernelFn tcg_kernel_for(int BS) {
 //   - K as the A operand: lane (r8, c) holds tokens r8 and r8 + 8 of an m-tile; head_dim is
 //     visited in the permuted order of the other fp8 kernel (lane c owns bytes [32c, 32c+32)
 //     of a row), shared with Q's B fragments.
-//   - V^T as the A operand: row r8 (and r8 + 8) of m-tile mt is head_dim element 16 r8 + 2 mt
-//     (and + 1), so a lane reads one 16-byte chunk per token row and pairs tokens with byte
-//     permutes (prmt) before the e4m3 -> f16 conversion.  The epilogue undoes the order.
+//   - The 16 tokens of an m-tile enter the MMAs in a permuted order: MMA row 2c is token 4c,
+//     2c + 1 is 4c + 1, 8 + 2c is 4c + 2 and 9 + 2c is 4c + 3 (c = 0..3), so the K rows a
+//     lane loads are tokens 2 r8 or 2 r8 - 1, and 2 r8 + 2 or 2 r8 + 1 (r8 even or odd).
+//   - V^T as the A operand: a transposing byte load (ldmatrix .b8 .trans) gives lane (r8, c)
+//     tokens 4c .. 4c + 3 of dims 16 md + r8 and 16 md + r8 + 8, which in that token order
+//     are exactly its A fragment after one e4m3 -> f16 conversion per 16-bit half.
 //   - P^T as the B operand: two movmatrix transposes per 16 tokens.
 template <int TR>
 __device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint32_t (&qb)[8][2],
@@ -1191,11 +1194,13 @@ __device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint3
                                            int valid, float scale_log2, int lane) {
   constexpr int MT = TR / 16;
   const int c = lane & 3, r8 = lane >> 2;
+  // tokens (within an m-tile) of the MMA rows r8 and r8 + 8 (the permuted order above)
+  const int tok_a = (r8 & 1) ? 2 * r8 - 1 : 2 * r8, tok_b = (r8 & 1) ? 2 * r8 + 1 : 2 * r8 + 2;
   float sc[MT][4];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.f;
-    const int ra = mt * 16 + r8, rb = ra + 8;
+    const int ra = mt * 16 + tok_a, rb = mt * 16 + tok_b;
     const uint4 a0 = lds128(kb + swz_chunk(ra, 2 * c)), a1 = lds128(kb + swz_chunk(ra, 2 * c + 1));
     const uint4 b0 = lds128(kb + swz_chunk(rb, 2 * c)), b1 = lds128(kb + swz_chunk(rb, 2 * c + 1));
     const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
@@ -1214,7 +1219,7 @@ __device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint3
   for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int tok = mt * 16 + r8 + (e >> 1) * 8;
+      const int tok = mt * 16 + ((e >> 1) ? tok_b : tok_a);
       const float v = sc[mt][e] * scale_log2;
       sc[mt][e] = tok < valid ? v : -INFINITY;
     }
@@ -1237,8 +1242,8 @@ __device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint3
     const float2 flo = Mma<__half>::unpack(lo), fhi = Mma<__half>::unpack(hi);
     rs0 += flo.x + fhi.x;
     rs1 += flo.y + fhi.y;
-    pb[mt][0] = movmatrix_trans(lo);  // (head r8, tokens 2c, 2c + 1)
-    pb[mt][1] = movmatrix_trans(hi);  // (head r8, tokens 8 + 2c, 9 + 2c)
+    pb[mt][0] = movmatrix_trans(lo);  // (head r8, MMA rows 2c, 2c + 1 = tokens 4c, 4c + 1)
+    pb[mt][1] = movmatrix_trans(hi);  // (head r8, MMA rows 8 + 2c, 9 + 2c = tokens 4c + 2, 4c + 3)
   }
   if (__any_sync(0xffffffffu, up0 || up1)) {
     const float a0 = fast_exp2(m[0] - mn0), a1 = fast_exp2(m[1] - mn1);  // 1 for heads that kept m
@@ -1256,26 +1261,17 @@ __device__ __forceinline__ void fp8g_block(uint32_t kb, uint32_t vb, const uint3
   m[1] = mn1;
   l[0] += rs0;
   l[1] += rs1;
-  // O^T += V^T . P^T
+  // O^T += V^T . P^T, m-tile md = dims 16 md .. 16 md + 15
 #pragma unroll
   for (int kt = 0; kt < MT; ++kt) {
-    const int t0 = kt * 16 + 2 * c;
-    const uint4 x0 = lds128(vb + swz_chunk(t0, r8)), x1 = lds128(vb + swz_chunk(t0 + 1, r8));
-    const uint4 x2 = lds128(vb + swz_chunk(t0 + 8, r8)), x3 = lds128(vb + swz_chunk(t0 + 9, r8));
-    const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
-    const uint32_t w2[4] = {x2.x, x2.y, x2.z, x2.w}, w3[4] = {x3.x, x3.y, x3.z, x3.w};
+    const int row = kt * 16 + (lane & 15);
 #pragma unroll
-    for (int qd = 0; qd < 4; ++qd) {
-      // head_dim 16 r8 + 4 qd + e, e = 0..3, for the token pairs (t0, t0+1) and (t0+8, t0+9)
-      uint32_t p[4], q[4];
-      e4m3x4_to_f16x2x2(__byte_perm(w0[qd], w1[qd], 0x5140), p[0], p[1]);
-      e4m3x4_to_f16x2x2(__byte_perm(w0[qd], w1[qd], 0x7362), p[2], p[3]);
-      e4m3x4_to_f16x2x2(__byte_perm(w2[qd], w3[qd], 0x5140), q[0], q[1]);
-      e4m3x4_to_f16x2x2(__byte_perm(w2[qd], w3[qd], 0x7362), q[2], q[3]);
-      const uint32_t fa0[4] = {p[0], p[1], q[0], q[1]};  // m-tile 2 qd
-      const uint32_t fa1[4] = {p[2], p[3], q[2], q[3]};  // m-tile 2 qd + 1
-      Mma<__half>::run(o[2 * qd], fa0, pb[kt][0], pb[kt][1]);
-      Mma<__half>::run(o[2 * qd + 1], fa1, pb[kt][0], pb[kt][1]);
+    for (int md = 0; md < 8; ++md) {
+      uint32_t x0, x1, fa[4];
+      ldsm_b8_trans(vb + swz_chunk(row, md), x0, x1);
+      e4m3x4_to_f16x2x2(x0, fa[0], fa[2]);  // dim 16 md + r8: tokens 4c, 4c + 1 | 4c + 2, 4c + 3
+      e4m3x4_to_f16x2x2(x1, fa[1], fa[3]);  // dim 16 md + r8 + 8
+      Mma<__half>::run(o[md], fa, pb[kt][0], pb[kt][1]);
     }
   }
 }
@@ -1355,15 +1351,15 @@ __global__ void __launch_bounds__(kThreads, 5)
       const int r8 = lane >> 2, c = lane & 3;
       const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int d = 16 * r8 + 2 * mt;  // rows r8 and r8 + 8 of m-tile mt: d and d + 1
+      for (int md = 0; md < 8; ++md) {
+        const int d = md * 16 + r8;  // rows r8 and r8 + 8 of m-tile md
         if (h0 < w.hc) {
-          O_s[(warp * HC + h0) * D + d] = o[mt][0];
-          O_s[(warp * HC + h0) * D + d + 1] = o[mt][2];
+          O_s[(warp * HC + h0) * D + d] = o[md][0];
+          O_s[(warp * HC + h0) * D + d + 8] = o[md][2];
         }
         if (h1 < w.hc) {
-          O_s[(warp * HC + h1) * D + d] = o[mt][1];
-          O_s[(warp * HC + h1) * D + d + 1] = o[mt][3];
+          O_s[(warp * HC + h1) * D + d] = o[md][1];
+          O_s[(warp * HC + h1) * D + d + 8] = o[md][3];
         }
       }
 #pragma unroll

@@ -144,6 +144,15 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "r"(addr));
 }
 
+// Transposing load of a 16 x 16 matrix of bytes (rows from the lanes' addresses, lanes 0-15
+// giving rows 0-15): lane t receives bytes of rows 4 (t % 4) .. 4 (t % 4) + 3, column t / 4
+// in r0 and column t / 4 + 8 in r1, row order from the low byte up.
+__device__ __forceinline__ void ldsm_b8_trans(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+
 template <typename T>
 struct Mma;
 
