@@ -50,15 +50,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each (the
     # timed step of `bench.py --steps 1 --warmup 3`)
-    "13b-mha-b64-bf16@2048": {"bytes": 1408782592 + 623360, "decode_cu_sha": "9560b5ee8e925ceb"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963332096 + 2517504, "decode_cu_sha": "9560b5ee8e925ceb"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328232960 + 1576704, "decode_cu_sha": "9560b5ee8e925ceb"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4300963840 + 32441344, "decode_cu_sha": "9560b5ee8e925ceb"},
-    "13b-mha-b64-bf16@4096+fp8": {"bytes": 704823296 + 2732800, "decode_cu_sha": "9560b5ee8e925ceb"},
-    "70b-gqa8-b128-bf16@4096+fp8": {"bytes": 482562560 + 2753280, "decode_cu_sha": "9560b5ee8e925ceb"},
-    "shared-prefix-cow-b256-bf16@4096+fp8": {"bytes": 164957696 + 1674240, "decode_cu_sha": "9560b5ee8e925ceb"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2151155968 + 40330752, "decode_cu_sha": "9560b5ee8e925ceb"},
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1968898048 + 20549888, "decode_cu_sha": "9560b5ee8e925ceb"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408782592 + 707072, "decode_cu_sha": "bbcc4be0c8206843"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963342848 + 2590976, "decode_cu_sha": "bbcc4be0c8206843"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328180224 + 1513984, "decode_cu_sha": "bbcc4be0c8206843"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4300875776 + 32241408, "decode_cu_sha": "bbcc4be0c8206843"},
+    "13b-mha-b64-bf16@4096+fp8": {"bytes": 705047552 + 565760, "decode_cu_sha": "bbcc4be0c8206843"},
+    "70b-gqa8-b128-bf16@4096+fp8": {"bytes": 482509312 + 1753856, "decode_cu_sha": "bbcc4be0c8206843"},
+    "shared-prefix-cow-b256-bf16@4096+fp8": {"bytes": 164953856 + 1230592, "decode_cu_sha": "bbcc4be0c8206843"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148249344 + 31764480, "decode_cu_sha": "bbcc4be0c8206843"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 2094713088 + 20505856, "decode_cu_sha": "bbcc4be0c8206843"},
 }
 
 
@@ -245,8 +245,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1392898816, "sources_sha": "5a92943affb3de81"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353465600, "sources_sha": "5a92943affb3de81"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1392890624, "sources_sha": "9ee5041f3cd3fae4"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353427200, "sources_sha": "9ee5041f3cd3fae4"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 
