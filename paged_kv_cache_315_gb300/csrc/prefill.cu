@@ -304,16 +304,18 @@ __global__ void __launch_bounds__(kUThreads, 2)
     int issued_mma = 0;
     auto pv = [&](int i) -> bool {  // O += P_i . V_i
       const int st = i % kUStages, b = i % SB;
-      int okp = 1;
-      if (lane == 0) okp = mbar_wait_bounded(smem_addr(&p_full[b]), (i / SB) & 1) ? 1 : 0;
-      okp = __shfl_sync(0xffffffffu, okp, 0);
-      // every lane observes the V tile's arrival (the warp may zero part of it)
-      const bool okv = okp && __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(&v_full[st]),
-                                                                         (i / kUStages) & 1));
-      if (!okv || __any_sync(0xffffffffu, flags[0] != 0)) {
-        if (lane == 0 && !okv) fail();
-        return false;
+      // lane 0 waits for P_i and V_i and reads the abort flag; one broadcast carries all
+      // three, and the __syncwarp after it orders the warp's zero-fill of stale V rows after
+      // the tile's arrival
+      int okv = 1;
+      if (lane == 0) {
+        okv = mbar_wait_bounded(smem_addr(&p_full[b]), (i / SB) & 1) ? 1 : 0;
+        if (okv) okv = mbar_wait_bounded(smem_addr(&v_full[st]), (i / kUStages) & 1) ? 1 : 0;
+        if (!okv) fail();
+        if (flags[0] != 0) okv = 0;
       }
+      if (!__shfl_sync(0xffffffffu, okv, 0)) return false;
+      __syncwarp();
       uint8_t* vt = ring + st * 2 * kUTile + kUTile;
       // value rows past the context (stale slots of the last block) become zeros before
       // they meet zero weights in P.V
@@ -355,25 +357,21 @@ __global__ void __launch_bounds__(kUThreads, 2)
     };
     for (int j = 0; ok && j < ntiles; ++j) {
       const int st = j % kUStages, b = j % SB;
+      // lane 0 waits for K_j and for S_b to be free, and reads the abort flag; one broadcast
+      // carries all three.  S_b still holds P_{j-SB}: the P.V that reads it must be complete
+      // before QK(j) overwrites it (that P.V is the ((j - SB) / SB)-th completion of
+      // pv_done[b]).
       int okk = 1;
-      if (lane == 0) okk = mbar_wait_bounded(smem_addr(&k_full[st]), (j / kUStages) & 1) ? 1 : 0;
-      okk = __shfl_sync(0xffffffffu, okk, 0);
-      if (!okk || __any_sync(0xffffffffu, flags[0] != 0)) {
-        if (lane == 0 && !okk) fail();
+      if (lane == 0) {
+        okk = mbar_wait_bounded(smem_addr(&k_full[st]), (j / kUStages) & 1) ? 1 : 0;
+        if (okk && j >= SB)
+          okk = mbar_wait_bounded(smem_addr(&pv_done[b]), ((j - SB) / SB) & 1) ? 1 : 0;
+        if (!okk) fail();
+        if (flags[0] != 0) okk = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, okk, 0)) {
         ok = 0;
         break;
-      }
-      // S_b still holds P_{j-SB}: the P.V that reads it must be complete before QK(j)
-      // overwrites it (that P.V is the ((j - SB) / SB)-th completion of pv_done[b])
-      if (j >= SB) {
-        int okv = 1;
-        if (lane == 0) okv = mbar_wait_bounded(smem_addr(&pv_done[b]), ((j - SB) / SB) & 1) ? 1 : 0;
-        okv = __shfl_sync(0xffffffffu, okv, 0);
-        if (!okv) {
-          if (lane == 0) fail();
-          ok = 0;
-          break;
-        }
       }
       const uint64_t dk = smem_desc_sw128(smem_addr(ring + st * 2 * kUTile), 16, 1024);
       if constexpr (WI) {
