@@ -245,8 +245,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1392890624, "sources_sha": "9ee5041f3cd3fae4"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353427200, "sources_sha": "9ee5041f3cd3fae4"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393013504, "sources_sha": "fd6ab4d975726f72"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353454848, "sources_sha": "fd6ab4d975726f72"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 
@@ -941,10 +941,10 @@ def run_swap(args) -> None:
 # batches (head_dim 128 and 64), from one ncu capture each, valid only for the kernel source
 # whose hash is recorded.
 PREFILL_TRAFFIC = {
-    "chunked-prefill-70b-gqa8-c512": {"bytes": 278717184 + 103227648,
-                                      "prefill_cu_sha": "5f787fdc73ef55bb"},
-    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139378432 + 36558080,
-                                          "prefill_cu_sha": "5f787fdc73ef55bb"},
+    "chunked-prefill-70b-gqa8-c512": {"bytes": 278775040 + 103675904,
+                                      "prefill_cu_sha": "81d2d13a8c16ff69"},
+    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139377920 + 36527616,
+                                          "prefill_cu_sha": "81d2d13a8c16ff69"},
 }
 
 

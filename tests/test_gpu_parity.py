@@ -310,6 +310,37 @@ def test_one_workspace_serves_changing_shapes(pkv):
         assert_close(host_out(out), oracle_decode(w), "bf16", f"shape {i}")
 
 
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,bs,part", [
+    ("bf16", 8, 8, 128, 16, 256),    # M = heads kernel, two partitions per CTA folded
+    ("bf16", 32, 8, 128, 32, 256),   # heads in N, two partitions per CTA, one partial each
+    ("f16", 64, 4, 64, 16, 512),     # 16-head chunks, head_dim 64
+    ("f32", 8, 2, 256, 16, 256),     # CUDA-core path
+])
+def test_split_contexts_from_a_dirty_workspace(pkv, dtype, Hq, Hkv, D, bs, part):
+    """Split contexts on every kernel family, with garbage in the workspace (work order and
+    partials) before each call: two calls give the oracle's result and identical bits (the
+    order in which CTAs finish does not change the merge)."""
+    lens = [1, 255, 256, 257, 511, 512, 513, 1400, 2048, 0, 3100, 777]
+    w = synth.make_workload("tm", seed=80 + D + bs, dtype=dtype, context_lens=lens,
+                            num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                            partition_size=part, key_outlier_frac=0.01)
+    t = synth.to_torch(w, "cuda")
+    need = pkv.paged_attn_decode_workspace_size(len(lens), Hq, Hkv, D, bs,
+                                                w.block_tables.shape[1], part)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        ws.random_(0, 256)
+        out = torch.full_like(t["q"], float("nan"))
+        pkv.paged_attn_decode(out, t["q"], t["k_cache"], t["v_cache"], t["block_tables"],
+                              t["context_lens"], w.scale, partition_size=part, workspace=ws)
+        assert pkv.pkv_device_error() == 0
+        outs.append(out)
+    assert_close(host_out(outs[0]), oracle_decode(w), dtype, f"{dtype} Hq{Hq} D{D} bs{bs}")
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_single_token_context_returns_v0_exactly(pkv):
     w = synth.make_workload("one", seed=13, dtype="bf16", context_lens=[1, 1, 1], num_q_heads=8,
                             num_kv_heads=2, head_dim=128, block_size=16)
