@@ -50,15 +50,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each (the
     # timed step of `bench.py --steps 1 --warmup 3`)
-    "13b-mha-b64-bf16@2048": {"bytes": 1408782592 + 707072, "decode_cu_sha": "bbcc4be0c8206843"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963342848 + 2590976, "decode_cu_sha": "bbcc4be0c8206843"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328180224 + 1513984, "decode_cu_sha": "bbcc4be0c8206843"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4300875776 + 32241408, "decode_cu_sha": "bbcc4be0c8206843"},
-    "13b-mha-b64-bf16@4096+fp8": {"bytes": 705047552 + 565760, "decode_cu_sha": "bbcc4be0c8206843"},
-    "70b-gqa8-b128-bf16@4096+fp8": {"bytes": 482509312 + 1753856, "decode_cu_sha": "bbcc4be0c8206843"},
-    "shared-prefix-cow-b256-bf16@4096+fp8": {"bytes": 164953856 + 1230592, "decode_cu_sha": "bbcc4be0c8206843"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148249344 + 31764480, "decode_cu_sha": "bbcc4be0c8206843"},
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 2094713088 + 20505856, "decode_cu_sha": "bbcc4be0c8206843"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408783360 + 711424, "decode_cu_sha": "6e1a0cc951a14054"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963338752 + 2689536, "decode_cu_sha": "6e1a0cc951a14054"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328227328 + 1829632, "decode_cu_sha": "6e1a0cc951a14054"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4300890624 + 32206592, "decode_cu_sha": "6e1a0cc951a14054"},
+    "13b-mha-b64-bf16@3072+fp8": {"bytes": 704766464 + 624384, "decode_cu_sha": "6e1a0cc951a14054"},
+    "70b-gqa8-b128-bf16@3072+fp8": {"bytes": 482739968 + 1078016, "decode_cu_sha": "6e1a0cc951a14054"},
+    "shared-prefix-cow-b256-bf16@3072+fp8": {"bytes": 164957952 + 1237504, "decode_cu_sha": "6e1a0cc951a14054"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148231936 + 31733504, "decode_cu_sha": "6e1a0cc951a14054"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 2096141312 + 20520960, "decode_cu_sha": "6e1a0cc951a14054"},
 }
 
 
@@ -245,8 +245,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393013504, "sources_sha": "fd6ab4d975726f72"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353454848, "sources_sha": "fd6ab4d975726f72"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1392970496, "sources_sha": "f104283636327049"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353405952, "sources_sha": "f104283636327049"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 

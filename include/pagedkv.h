@@ -235,8 +235,8 @@ int paged_attn_prefill(void* out, const void* q, const void* k_cache, const void
  * num_kv_heads * head_dim * 2 element bytes, keys and values) exceed the L2 cache (about
  * 126 MB on GB300): then plain decode reads every member's copy of the prefix from HBM.
  * Measured on one GB300: 64 prompts of 4096 tokens shared by 8 sequences each (1 GB of
- * prefix) ran x1.80 faster than paged_attn_decode; 256 sequences sharing one 992-token
- * prefix (4 MB, held in L2 across the batch) ran x0.95 as fast.
+ * prefix) ran x1.79 faster than paged_attn_decode; 256 sequences sharing one 992-token
+ * prefix (4 MB, held in L2 across the batch) ran x0.92 as fast.
  * Returns PKV_OK, PKV_EINVAL, PKV_ENOMEM, PKV_EUNSUPPORTED or PKV_ECUDA.
  */
 size_t paged_attn_decode_shared_prefix_workspace_size(int num_seqs, int num_groups,
@@ -267,11 +267,11 @@ int paged_attn_decode_shared_prefix(void* out, const void* q, const void* k_cach
  * q and out are `dtype` (PKV_BF16 or PKV_F16).  Codes convert exactly to fp16, so the
  * products run on the tensor cores in fp16 with fp32 accumulation.  head_dim must be 128
  * and block_size 16, 32 or 64.  Other arguments, the workspace and the return codes are
- * those of paged_attn_decode, except the default partition (partition_size 0): at one
- * byte per element a token carries half the bytes, so the candidates double to 4096,
- * 2048 and 1024 tokens (same 2048-work-unit rule).  The workspace is sized by
- * paged_attn_decode_fp8_workspace_size (never more than paged_attn_decode_workspace_size
- * for the same arguments).
+ * those of paged_attn_decode, except the default partition (partition_size 0): the
+ * candidates grow by half to 3072, 1536 and 768 tokens (same 2048-work-unit rule).  At
+ * one byte per element a token carries half the bytes, but its conversions cost more
+ * instructions, and a 1.5x unit takes about as long as a 16-bit one.  The workspace is
+ * sized by paged_attn_decode_fp8_workspace_size.
  */
 int paged_attn_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, const int32_t* context_lens, int num_seqs,

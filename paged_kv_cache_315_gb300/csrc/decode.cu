@@ -1625,19 +1625,20 @@ int resolve_partition_tokens(int partition_size, int block_size, int num_seqs, i
                              int num_kv_heads, int max_blocks_per_seq, int kv_elem_bytes) {
   if (block_size <= 0) return -1;
   if (partition_size == 0) {
-    // The largest of 2048, 1024, 512 tokens (x2 for 1-byte E4M3 elements, so a work unit
-    // carries the same bytes) that still leaves at least kMinUnits work units (sequence x
-    // KV head x 16-head chunk x partition, counting every sequence at the block table's
-    // full length); longer partitions amortise each CTA's start-up cost, shorter ones
-    // balance uneven contexts across the SMs.
+    // The largest of 2048, 1024, 512 tokens that still leaves at least kMinUnits work units
+    // (sequence x KV head x 16-head chunk x partition, counting every sequence at the block
+    // table's full length); longer partitions amortise each CTA's start-up cost, shorter
+    // ones balance uneven contexts across the SMs.  For 1-byte E4M3 elements the candidates
+    // grow by half: a token carries half the bytes, but its conversions cost more
+    // instructions, and a 1.5x unit takes about as long as a 16-bit one.
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
     const int group = num_kv_heads > 0 ? std::max(1, num_q_heads / num_kv_heads) : 1;
     const long long heads = static_cast<long long>(std::max(0, num_seqs)) *
                             std::max(1, num_kv_heads) * ((group + kTcHeads - 1) / kTcHeads);
-    const int widen = kv_elem_bytes == 1 ? 2 : 1;
+    const int widen2 = kv_elem_bytes == 1 ? 3 : 2;  // twice the widening factor
     int t = 0;
     for (int cand : {2048, 1024, kDefaultPartitionTokens}) {
-      t = std::max(block_size, (widen * cand / block_size) * block_size);
+      t = std::max(block_size, (widen2 * cand / 2 / block_size) * block_size);
       if (heads * ((max_ctx + t - 1) / t) >= kMinUnits) break;
     }
     return t;

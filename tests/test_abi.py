@@ -136,26 +136,30 @@ def test_default_partition_size_follows_available_parallelism(lib):
         pkv.paged_attn_decode_workspace_size(4, 32, 8, 128, 16, 2048, 512)
 
 
-def test_fp8_default_partition_carries_the_bytes_of_the_16_bit_one(lib):
-    """At one byte per element the default candidates double (4096, 2048, 1024 tokens)
-    under the same 2048-work-unit rule; explicit sizes are kept."""
+def test_fp8_default_partition_is_one_and_a_half_of_the_16_bit_one(lib):
+    """At one byte per element the default candidates grow by half (3072, 1536, 768
+    tokens) under the same 2048-work-unit rule; explicit sizes are kept."""
     import paged_kv_cache_315_gb300 as pkv
 
     f8, f16 = pkv.paged_attn_decode_fp8_partition_tokens, pkv.paged_attn_decode_partition_tokens
-    # 128 seqs x 8 KV heads x 2 partitions of 4096 (8192-token tables) = 2048 units
+    # 128 seqs x 8 KV heads x 3 partitions of 3072 (8192-token tables) = 3072 units
     assert f16(128, 64, 8, 16, 512, 0) == 2048
-    assert f8(128, 64, 8, 16, 512, 0) == 4096
-    # 1024 (seq, head) pairs over 2048-token tables: 4096 and 2048 give one partition each
-    # (1024 units), 1024 gives two
-    assert f8(128, 64, 8, 16, 128, 0) == 1024
-    assert f8(4, 32, 8, 16, 2048, 0) == 1024
+    assert f8(128, 64, 8, 16, 512, 0) == 3072
+    # 1024 (seq, head) pairs over 2048-token tables: 3072 gives one partition each (1024
+    # units), 1536 gives two
+    assert f8(128, 64, 8, 16, 128, 0) == 1536
+    # 32 (seq, head) pairs over 32768-token tables: no candidate reaches 2048 units, so
+    # the smallest, 768, is taken
+    assert f8(4, 32, 8, 16, 2048, 0) == 768
+    # block sizes that do not divide 1.5 x 2048 evenly round each candidate down
+    assert f8(64, 40, 40, 48, 64, 0) == 3072 - 3072 % 48
     assert f8(32, 32, 8, 16, 2048, 512) == 512
     assert f8(64, 40, 40, 48, 64, 0) % 48 == 0
     with pytest.raises(pkv.PagedKVError):
         f8(32, 32, 8, 16, 2048, 100)
-    # the workspace follows the fp8 choice and never exceeds the 16-bit one
+    # the workspace follows the fp8 choice
     ws8, ws16 = pkv.paged_attn_decode_fp8_workspace_size, pkv.paged_attn_decode_workspace_size
-    assert ws8(128, 64, 8, 128, 16, 512, 0) == ws16(128, 64, 8, 128, 16, 512, 4096)
+    assert ws8(128, 64, 8, 128, 16, 512, 0) == ws16(128, 64, 8, 128, 16, 512, 3072)
     assert ws8(128, 64, 8, 128, 16, 512, 0) < ws16(128, 64, 8, 128, 16, 512, 0)
     assert ws8(4, 32, 8, 128, 16, 2048, 512) == ws16(4, 32, 8, 128, 16, 2048, 512)
 
