@@ -245,8 +245,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1392970496, "sources_sha": "f104283636327049"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353405952, "sources_sha": "f104283636327049"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393198336, "sources_sha": "72db41b3ff633a6d"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353478400, "sources_sha": "72db41b3ff633a6d"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 
@@ -941,10 +941,10 @@ def run_swap(args) -> None:
 # batches (head_dim 128 and 64), from one ncu capture each, valid only for the kernel source
 # whose hash is recorded.
 PREFILL_TRAFFIC = {
-    "chunked-prefill-70b-gqa8-c512": {"bytes": 278775040 + 103675904,
-                                      "prefill_cu_sha": "81d2d13a8c16ff69"},
-    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139377920 + 36527616,
-                                          "prefill_cu_sha": "81d2d13a8c16ff69"},
+    "chunked-prefill-70b-gqa8-c512": {"bytes": 278723328 + 103297792,
+                                      "prefill_cu_sha": "9170c7eb63908a79"},
+    "chunked-prefill-70b-gqa8-c512-d64": {"bytes": 139379968 + 36869120,
+                                          "prefill_cu_sha": "9170c7eb63908a79"},
 }
 
 

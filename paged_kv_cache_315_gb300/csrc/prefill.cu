@@ -94,14 +94,16 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
 constexpr int kUThreads = 224;
 constexpr int kURows = 128;       // packed query rows per CTA
 constexpr int kUKeys = 64;        // key tokens per tile
-constexpr int kUStages = 2;       // K/V ring depth
+constexpr int kUStages = 2;       // K/V ring depth at head_dim 128 (shared memory allows no more)
 constexpr int kUTmemCols = 256;
 // bytes of a K (or V) tile, of the Q tile, and the dynamic shared memory, for head_dim D
 // (D / 64 boxes of 64 columns per row, each box 128-byte rows)
 __host__ __device__ constexpr int u_tile(int D) { return kUKeys * D * 2; }
 __host__ __device__ constexpr int u_qbytes(int D) { return kURows * D * 2; }
+// K/V ring depth: head_dim 64 tiles take half the bytes, so the rings run deeper
+__host__ __device__ constexpr int u_stages(int D) { return D == 64 ? 3 : kUStages; }
 __host__ __device__ constexpr int u_smem(int D) {
-  return 1024 + u_qbytes(D) + kUStages * 2 * u_tile(D) + 256;
+  return 1024 + u_qbytes(D) + u_stages(D) * 2 * u_tile(D) + 512;
 }
 
 template <typename T, int D, int BS, bool QT, bool WI>
@@ -114,12 +116,15 @@ __global__ void __launch_bounds__(kUThreads, 2)
   constexpr int NBX = D / 64;                  // 64-column boxes per row
   constexpr int kUTile = u_tile(D);
   constexpr int kUQBytes = u_qbytes(D);
+  constexpr int ST = u_stages(D);
   constexpr bool kBf16 = sizeof(T) == 2 && !std::is_same<T, __half>::value;
   constexpr uint32_t kIdQK = umma_idesc(kURows, kUKeys, kBf16, false);
   constexpr uint32_t kIdPV = umma_idesc(kURows, D, kBf16, true);
   // score buffers: at head_dim 64 the output takes 64 columns, so a third 64-column buffer
   // fits in the CTA's 256 (QK(j) then waits for PV(j - 3) instead of PV(j - 2))
   constexpr int SB = D == 64 ? 3 : 2;
+  // barriers, the tensor-memory address and the flags fit the 512 bytes past the ring
+  static_assert((2 + 4 * ST + 3 * SB) * 8 + 16 <= 512, "barrier area");
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -173,13 +178,13 @@ __global__ void __launch_bounds__(kUThreads, 2)
   uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sq = base;
   uint8_t* ring = base + kUQBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kUStages * 2 * kUTile);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + ST * 2 * kUTile);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;                   // [kUStages]
-  uint64_t* k_empty = k_full + kUStages;         // [kUStages]
-  uint64_t* v_full = k_empty + kUStages;         // [kUStages]
-  uint64_t* v_empty = v_full + kUStages;         // [kUStages]
-  uint64_t* s_full = v_empty + kUStages;         // [SB]
+  uint64_t* k_full = bars + 1;                   // [ST]
+  uint64_t* k_empty = k_full + ST;               // [ST]
+  uint64_t* v_full = k_empty + ST;               // [ST]
+  uint64_t* v_empty = v_full + ST;               // [ST]
+  uint64_t* s_full = v_empty + ST;               // [SB]
   uint64_t* p_full = s_full + SB;                // [SB]
   uint64_t* pv_done = p_full + SB;               // [SB]: the P.V of the tiles using S_b
   uint64_t* drain = pv_done + SB;
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(kUThreads, 2)
 
   if (tid == 0) {
     mbar_init(smem_addr(q_full), QT ? 4 : 1);  // QT: one arrival per softmax warp
-    for (int i = 0; i < kUStages; ++i) {
+    for (int i = 0; i < ST; ++i) {
       mbar_init(smem_addr(&k_full[i]), 1);
       mbar_init(smem_addr(&k_empty[i]), 1);
       mbar_init(smem_addr(&v_full[i]), 1);
@@ -264,12 +269,12 @@ __global__ void __launch_bounds__(kUThreads, 2)
     int issued = 0;
     int ynext = ntiles > 0 ? row_of(0) : 0;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j % kUStages;
+      const int st = j % ST;
       const int y = ynext;
       if (j + 1 < ntiles) ynext = row_of(j + 1);
       int ok = 1;
-      if (lane == 0 && j >= kUStages)
-        ok = mbar_wait_bounded(smem_addr(&emptyb[st]), ((j / kUStages) - 1) & 1) ? 1 : 0;
+      if (lane == 0 && j >= ST)
+        ok = mbar_wait_bounded(smem_addr(&emptyb[st]), ((j / ST) - 1) & 1) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok || __any_sync(0xffffffffu, flags[0] != 0)) {
         if (lane == 0 && !ok) fail();
@@ -303,14 +308,14 @@ __global__ void __launch_bounds__(kUThreads, 2)
     if (!ok && lane == 0) fail();
     int issued_mma = 0;
     auto pv = [&](int i) -> bool {  // O += P_i . V_i
-      const int st = i % kUStages, b = i % SB;
+      const int st = i % ST, b = i % SB;
       // lane 0 waits for P_i and V_i and reads the abort flag; one broadcast carries all
       // three, and the __syncwarp after it orders the warp's zero-fill of stale V rows after
       // the tile's arrival
       int okv = 1;
       if (lane == 0) {
         okv = mbar_wait_bounded(smem_addr(&p_full[b]), (i / SB) & 1) ? 1 : 0;
-        if (okv) okv = mbar_wait_bounded(smem_addr(&v_full[st]), (i / kUStages) & 1) ? 1 : 0;
+        if (okv) okv = mbar_wait_bounded(smem_addr(&v_full[st]), (i / ST) & 1) ? 1 : 0;
         if (!okv) fail();
         if (flags[0] != 0) okv = 0;
       }
@@ -356,14 +361,14 @@ __global__ void __launch_bounds__(kUThreads, 2)
       return true;
     };
     for (int j = 0; ok && j < ntiles; ++j) {
-      const int st = j % kUStages, b = j % SB;
+      const int st = j % ST, b = j % SB;
       // lane 0 waits for K_j and for S_b to be free, and reads the abort flag; one broadcast
       // carries all three.  S_b still holds P_{j-SB}: the P.V that reads it must be complete
       // before QK(j) overwrites it (that P.V is the ((j - SB) / SB)-th completion of
       // pv_done[b]).
       int okk = 1;
       if (lane == 0) {
-        okk = mbar_wait_bounded(smem_addr(&k_full[st]), (j / kUStages) & 1) ? 1 : 0;
+        okk = mbar_wait_bounded(smem_addr(&k_full[st]), (j / ST) & 1) ? 1 : 0;
         if (okk && j >= SB)
           okk = mbar_wait_bounded(smem_addr(&pv_done[b]), ((j - SB) / SB) & 1) ? 1 : 0;
         if (!okk) fail();
@@ -600,8 +605,8 @@ __global__ void __launch_bounds__(kUThreads, 2)
     if (is_k && !QT) mbar_wait_bounded(smem_addr(q_full), 0);
     uint64_t* fullb = is_k ? k_full : v_full;
     const int issued = flags[is_k ? 1 : 2];
-    for (int j = max(0, issued - kUStages); j < issued; ++j)
-      mbar_wait_bounded(smem_addr(&fullb[j % kUStages]), (j / kUStages) & 1);
+    for (int j = max(0, issued - ST); j < issued; ++j)
+      mbar_wait_bounded(smem_addr(&fullb[j % ST]), (j / ST) & 1);
   }
   tc_fence_before_sync();
   __syncthreads();
