@@ -1446,7 +1446,16 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int n = num_seqs * groups;
   for (int b = tid; b < nbins; b += kPrepThreads) bins[b] = 0;
   __syncthreads();
-  for (int i = tid; i < n; i += kPrepThreads)
+  // the counts of this thread's first kCached items stay in registers for the second pass
+  constexpr int kCached = 2;
+  int cached[kCached];
+#pragma unroll
+  for (int k = 0; k < kCached; ++k) {
+    const int i = tid + k * kPrepThreads;
+    cached[k] = i < n ? item_blocks(context_lens, i, groups, group_tokens, block_size, max_len) : 0;
+    if (i < n) atomicAdd(&bins[gblocks - cached[k]], 1);
+  }
+  for (int i = tid + kCached * kPrepThreads; i < n; i += kPrepThreads)
     atomicAdd(&bins[gblocks - item_blocks(context_lens, i, groups, group_tokens, block_size,
                                            max_len)], 1);
   __syncthreads();
@@ -1480,7 +1489,12 @@ __global__ void __launch_bounds__(kPrepThreads)
     base += c;
   }
   __syncthreads();
-  for (int i = tid; i < n; i += kPrepThreads)
+#pragma unroll
+  for (int k = 0; k < kCached; ++k) {
+    const int i = tid + k * kPrepThreads;
+    if (i < n) order[atomicAdd(&bins[gblocks - cached[k]], 1)] = i;
+  }
+  for (int i = tid + kCached * kPrepThreads; i < n; i += kPrepThreads)
     order[atomicAdd(&bins[gblocks - item_blocks(context_lens, i, groups, group_tokens, block_size,
                                                 max_len)], 1)] = i;
 }
@@ -1517,42 +1531,72 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Pa
   griddep_wait();
   if (np <= 1) return;
   const size_t base = static_cast<size_t>(row) * P.max_parts;
-  const float* ml = P.ws_ml + base * 2;
-  float M = -INFINITY;
-  for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(&ml[2 * p]));
+  const float2* ml = reinterpret_cast<const float2*>(P.ws_ml) + base;
+  const float* o = P.ws_o + base * D + lane * V;
+  auto load_cols = [&](int p, float (&x)[V]) {
+    const float* src = o + static_cast<size_t>(p) * D;
+    if constexpr (V % 4 == 0) {
+#pragma unroll
+      for (int k = 0; k < V; k += 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + k));
+        x[k] = v.x;
+        x[k + 1] = v.y;
+        x[k + 2] = v.z;
+        x[k + 3] = v.w;
+      }
+    } else if constexpr (V == 2) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+      x[0] = v.x;
+      x[1] = v.y;
+    } else {
+      x[0] = __ldcg(src);
+    }
+  };
+  // The first 32 partials' (m, l), one per lane, and the first kPre partials' columns are
+  // loaded together, before any of the arithmetic that waits for them.
+  constexpr int kPre = D >= 256 ? 4 : 8;
+  const float2 first = lane < np ? __ldcg(&ml[lane]) : make_float2(-INFINITY, 0.f);
+  float pre[kPre][V];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i)
+    if (i < np) load_cols(i, pre[i]);
+  float M = first.x;
+  for (int p = lane + 32; p < np; p += 32) M = fmaxf(M, __ldcg(&ml[p]).x);
   M = warp_max(M);
-  float den = 0.f;
-  for (int p = lane; p < np; p += 32) den += exp2f(__ldcg(&ml[2 * p]) - M) * __ldcg(&ml[2 * p + 1]);
+  float den = lane < np ? exp2f(first.x - M) * first.y : 0.f;
+  for (int p = lane + 32; p < np; p += 32) {
+    const float2 v = __ldcg(&ml[p]);
+    den += exp2f(v.x - M) * v.y;
+  }
   den = warp_sum(den);
   const float inv = 1.f / den;
   float acc[V];
 #pragma unroll
   for (int k = 0; k < V; ++k) acc[k] = 0.f;
-  const float* o = P.ws_o + base * D + lane * V;
   for (int p0 = 0; p0 < np; p0 += 32) {
     const int p = p0 + lane;
-    const float wp = p < np ? exp2f(__ldcg(&ml[2 * p]) - M) * inv : 0.f;
+    const float mp = p0 == 0 ? first.x : (p < np ? __ldcg(&ml[p]).x : -INFINITY);
+    const float wp = p < np ? exp2f(mp - M) * inv : 0.f;
     const int cnt = min(32, np - p0);
-#pragma unroll 8
-    for (int i = 0; i < cnt; ++i) {
-      const float wi = __shfl_sync(0xffffffffu, wp, i);
-      const float* src = o + static_cast<size_t>(p0 + i) * D;
-      if constexpr (V % 4 == 0) {
+    int i = 0;
+    if (p0 == 0) {
 #pragma unroll
-        for (int k = 0; k < V; k += 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + k));
-          acc[k] += wi * x.x;
-          acc[k + 1] += wi * x.y;
-          acc[k + 2] += wi * x.z;
-          acc[k + 3] += wi * x.w;
+      for (int j = 0; j < kPre; ++j) {
+        const float wi = __shfl_sync(0xffffffffu, wp, j);
+        if (j < cnt) {
+#pragma unroll
+          for (int k = 0; k < V; ++k) acc[k] += wi * pre[j][k];
         }
-      } else if constexpr (V == 2) {
-        const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-        acc[0] += wi * x.x;
-        acc[1] += wi * x.y;
-      } else {
-        acc[0] += wi * __ldcg(src);
       }
+      i = kPre;
+    }
+#pragma unroll 8
+    for (; i < cnt; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, wp, i);
+      float x[V];
+      load_cols(p0 + i, x);
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] += wi * x[k];
     }
   }
   T* out = static_cast<T*>(P.out) + static_cast<size_t>(row) * D + lane * V;
