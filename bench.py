@@ -50,15 +50,15 @@ FALLBACK_BF16_TFLOPS = 1900.0
 MEASURED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one decode launch each (the
     # timed step of `bench.py --steps 1 --warmup 3`)
-    "13b-mha-b64-bf16@2048": {"bytes": 1408783360 + 711424, "decode_cu_sha": "6e1a0cc951a14054"},
-    "70b-gqa8-b128-bf16@2048": {"bytes": 963338752 + 2689536, "decode_cu_sha": "6e1a0cc951a14054"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328227328 + 1829632, "decode_cu_sha": "6e1a0cc951a14054"},
-    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4300890624 + 32206592, "decode_cu_sha": "6e1a0cc951a14054"},
-    "13b-mha-b64-bf16@3072+fp8": {"bytes": 704766464 + 624384, "decode_cu_sha": "6e1a0cc951a14054"},
-    "70b-gqa8-b128-bf16@3072+fp8": {"bytes": 482739968 + 1078016, "decode_cu_sha": "6e1a0cc951a14054"},
-    "shared-prefix-cow-b256-bf16@3072+fp8": {"bytes": 164957952 + 1237504, "decode_cu_sha": "6e1a0cc951a14054"},
-    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148231936 + 31733504, "decode_cu_sha": "6e1a0cc951a14054"},
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 2096141312 + 20520960, "decode_cu_sha": "6e1a0cc951a14054"},
+    "13b-mha-b64-bf16@2048": {"bytes": 1408783360 + 626944, "decode_cu_sha": "03c89ed11f9bee50"},
+    "70b-gqa8-b128-bf16@2048": {"bytes": 963344896 + 2590208, "decode_cu_sha": "03c89ed11f9bee50"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 328271616 + 1593856, "decode_cu_sha": "03c89ed11f9bee50"},
+    "longctx-32k-gqa4-b32-bf16@512": {"bytes": 4300867584 + 32169728, "decode_cu_sha": "03c89ed11f9bee50"},
+    "13b-mha-b64-bf16@3072+fp8": {"bytes": 704773376 + 552448, "decode_cu_sha": "03c89ed11f9bee50"},
+    "70b-gqa8-b128-bf16@3072+fp8": {"bytes": 482749440 + 1077760, "decode_cu_sha": "03c89ed11f9bee50"},
+    "shared-prefix-cow-b256-bf16@3072+fp8": {"bytes": 164968448 + 1629440, "decode_cu_sha": "03c89ed11f9bee50"},
+    "longctx-32k-gqa4-b32-bf16@512+fp8": {"bytes": 2148399616 + 31738368, "decode_cu_sha": "03c89ed11f9bee50"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1984763136 + 20503552, "decode_cu_sha": "03c89ed11f9bee50"},
 }
 
 
@@ -245,8 +245,8 @@ class ClockSampler:
 # DRAM bytes of one shared-prefix cascade call (every kernel of the call: prep, prefix pass,
 # suffix ordering and decode, merge), valid only for the recorded sources
 CASCADE_TRAFFIC: dict = {
-    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1393198336, "sources_sha": "72db41b3ff633a6d"},
-    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353478400, "sources_sha": "72db41b3ff633a6d"},
+    "grouped-prefix-64x8-p4096-bf16@2048": {"bytes": 1392939264, "sources_sha": "6b6ab9135d74ca0c"},
+    "shared-prefix-cow-b256-bf16@2048": {"bytes": 353472768, "sources_sha": "6b6ab9135d74ca0c"},
 }
 CASCADE_SOURCES = ("prefill.cu", "decode.cu", "shared_prefix.cu")
 

@@ -235,7 +235,7 @@ int paged_attn_prefill(void* out, const void* q, const void* k_cache, const void
  * num_kv_heads * head_dim * 2 element bytes, keys and values) exceed the L2 cache (about
  * 126 MB on GB300): then plain decode reads every member's copy of the prefix from HBM.
  * Measured on one GB300: 64 prompts of 4096 tokens shared by 8 sequences each (1 GB of
- * prefix) ran x1.79 faster than paged_attn_decode; 256 sequences sharing one 992-token
+ * prefix) ran x1.77 faster than paged_attn_decode; 256 sequences sharing one 992-token
  * prefix (4 MB, held in L2 across the batch) ran x0.92 as fast.
  * Returns PKV_OK, PKV_EINVAL, PKV_ENOMEM, PKV_EUNSUPPORTED or PKV_ECUDA.
  */
